@@ -1,0 +1,419 @@
+"""Benchmark: one step = build the topology CSR from K, then scheduled attention over it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {tsa,reference}]
+                    [--workload NAME] [--schedule topology|dense|density:P]
+
+Metric: scheduled-attention forward TFLOP/s counted on visited blocks
+(nnz * lanes * 4 * 64^2 * D per step) and ms per step.  Default workload: [B=2, H=32,
+S=32768, D=128] bf16, block 64, sink 2, local_radius 4, topk 8, keys clustered over 32
+means (the S 32768 configuration).  Inputs are synthetic, seeded, resident in HBM and larger
+than L2 (no flush needed).  Under torchrun every rank runs its own independent problem
+(seed = rank): weak scaling, no collective on the data path.
+
+--impl reference times the CPU oracle (oracle/, fp64) on the host cores on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from topology_scheduled_gb300.workloads import WORKLOADS, make_qkv, random_density_csr  # noqa: E402
+
+DEFAULT_WORKLOAD = "b2h32s32768"
+ATTN_SOURCE = os.path.join(ROOT, "topology_scheduled_gb300", "csrc", "attention.cu")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["tsa", "reference"], default="tsa")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    p.add_argument("--schedule", default="topology")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="target CPU time of the oracle's attention sample")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def visited_flops(nnz: int, lanes: int, D: int, block: int = 64) -> float:
+    return float(nnz) * lanes * 4.0 * block * block * D
+
+
+def dtype_name(dt) -> str:
+    return {torch.float16: "f16", torch.bfloat16: "bf16"}[dt]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def attention_traffic_per_launch(workload: str, schedule: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it matches the source."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    with open(ATTN_SOURCE, "rb") as f:
+        digest = hashlib.sha1(f.read()).hexdigest()
+    entry = rec.get(f"{workload}/{schedule}")
+    if not entry or entry.get("attention_cu_sha1") != digest:
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def build_schedule_host(w, schedule: str):
+    """CSR for non-topology schedules (host-built inputs, copied once before timing)."""
+    if schedule == "dense":
+        return None
+    if schedule.startswith("density:"):
+        return random_density_csr(w.nb, float(schedule.split(":")[1]), 0)
+    raise ValueError(schedule)
+
+
+def run_gpu(args):
+    import torch.distributed as dist
+
+    import topology_scheduled_gb300 as tsa
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream()
+    q, k, v = make_qkv(w, seed=rank, device=dev)
+    out = torch.empty_like(q)
+    cap = tsa.tsa_schedule_max_nnz(w.S, w.block, w.sink, w.local_radius, w.topk)
+    ws = torch.empty(tsa.tsa_build_schedule_workspace_bytes(w.lanes, w.S, w.D, w.block),
+                     dtype=torch.uint8, device=dev)
+    topo = args.schedule == "topology"
+    if topo:
+        row_ptr = torch.empty(w.nb + 1, dtype=torch.int32, device=dev)
+        col_idx = torch.empty(cap, dtype=torch.int32, device=dev)
+    elif args.schedule == "dense":
+        row_ptr, col_idx = tsa.tsa_dense_causal_csr(w.S, w.block, device=dev)
+    else:
+        rp, ci = build_schedule_host(w, args.schedule)
+        row_ptr, col_idx = torch.as_tensor(rp, device=dev), torch.as_tensor(ci, device=dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(attn_events=None, build_events=None):
+        if topo:
+            if build_events:
+                build_events[0].record(stream)
+            tsa.tsa_build_schedule(k, w.block, w.sink, w.local_radius, w.topk, workspace=ws,
+                                   row_ptr=row_ptr, col_idx=col_idx)
+            if build_events:
+                build_events[1].record(stream)
+        if attn_events:
+            attn_events[0].record(stream)
+        tsa.tsa_scheduled_attention(q, k, v, row_ptr, col_idx, w.scale, out=out)
+        if attn_events:
+            attn_events[1].record(stream)
+
+    step()
+    status = tsa.tsa_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {tsa.STATUS_NAMES.get(status, status)}")
+    nnz = int(row_ptr[-1].item())
+    flops = visited_flops(nnz, w.lanes, w.D, w.block)
+    launches_per_step = 1 + (6 + 2 * math.ceil(math.log2(w.nb)) if topo else 0)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+
+    attn_ev = [(ev(), ev()) for _ in range(args.steps)]
+    build_ev = [(ev(), ev()) for _ in range(args.steps)] if topo else [None] * args.steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    wall0 = time.perf_counter()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(attn_ev[i], build_ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    status = tsa.tsa_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timing {tsa.STATUS_NAMES.get(status, status)}")
+    elapsed_ms = t0.elapsed_time(t1)
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    build_ms = [a.elapsed_time(b) for a, b in build_ev] if topo else [0.0]
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+        tot = torch.tensor([flops], device=dev, dtype=torch.float64)
+        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+        flops_all = float(tot.item())
+    else:
+        flops_all = flops
+    ms_per_step = elapsed_ms / args.steps
+    value = flops_all * args.steps / (elapsed_ms * 1e-3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, tsa, q, k, v, out, ws, row_ptr, col_idx, topo, flops, stream, world)
+
+    peaks, peak_kind = measured_peaks()
+    attn_mean = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    if w.dtype == torch.float16:
+        pass  # dense f16 and bf16 tensor rates are the same on this part
+    traffic = attention_traffic_per_launch(args.workload, args.schedule)
+    line = {
+        "metric": "scheduled-attn fwd TFLOP/s on visited blocks (% of GB300 bf16 peak); ms/call",
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": dtype_name(w.dtype),
+        "data": "synthetic (seeded N(0,1) Q/V, clustered K; no dataset)",
+        "config": {
+            "workload": f"{args.workload}: {w.describe()}",
+            "schedule": args.schedule,
+            "B": w.B, "H": w.H, "S": w.S, "D": w.D, "block": w.block,
+            "nnz_blocks": nnz, "dense_blocks": w.nb * (w.nb + 1) // 2,
+            "visited_flops_per_step": flops,
+            "l2": "inputs larger than L2 (Q,K,V,O %.2f GB per rank), no flush"
+                  % (4 * q.numel() * q.element_size() / 1e9),
+            "parallelism": f"independent problem per rank x{world} (no collective)",
+        },
+        "breakdown": {
+            "attention_ms": round(attn_mean, 4),
+            "attention_tflops": round(achieved, 3),
+            "build_ms": round(statistics.mean(build_ms), 4),
+            "pct_of_bf16_peak_step": round(100.0 * value / world / peak, 2),
+            "wall_s_timed_region": round(wall, 3),
+        },
+        "roofline": {
+            "kernel": "scheduled_attention_kernel",
+            "bound": "tensor",
+            "achieved": round(achieved, 3),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} bf16_tflops_sustained (cuBLAS bf16, seconds-long loop)",
+            "traffic": traffic,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, w, q.cpu(), k.cpu(), v.cpu(), row_ptr, col_idx, topo)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, tsa, q, k, v, out, ws, row_ptr, col_idx, topo, flops, stream, world):
+    """Same step through the public API from pinned host buffers, copies inside the timing."""
+    steps = max(1, min(args.steps, 5))
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    hnnz = torch.empty(1, dtype=torch.int32, pin_memory=True)
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        if topo:
+            tsa.tsa_build_schedule(k, w.block, w.sink, w.local_radius, w.topk, workspace=ws,
+                                   row_ptr=row_ptr, col_idx=col_idx)
+        tsa.tsa_scheduled_attention(q, k, v, row_ptr, col_idx, w.scale, out=out)
+        ho.copy_(out, non_blocking=True)
+        hnnz.copy_(row_ptr[-1:], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = out.numel() * out.element_size() + 4
+    return {"value": round(flops * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 3), "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo):
+    """The fp64 CPU oracle on the host cores: full schedule build + a sample of attention rows."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    S, D = w.S, w.D
+    kh = k.reshape(-1, S, D)
+    t0 = time.perf_counter()
+    if topo:
+        rp, ci, _ = oracle.build_schedule(kh, w.block, w.sink, w.local_radius, w.topk)
+    else:
+        rp = row_ptr.cpu().numpy()
+        ci = col_idx.cpu().numpy()[: rp[-1]]
+    t_build = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    qh, vh = q.reshape(-1, S, D), v.reshape(-1, S, D)
+    lens = np.diff(rp).astype(np.float64)
+    n = 512
+    done_rows, done_flops, t_attn = 0, 0.0, 0.0
+    while t_attn < args.cpu_seconds:
+        lanes = rng.integers(0, w.lanes, n).astype(np.int64)
+        toks = rng.integers(0, S, n).astype(np.int64)
+        t1 = time.perf_counter()
+        oracle.attention(qh, kh, vh, rp, ci, w.block, w.scale, lanes=lanes, tokens=toks, nthreads=threads)
+        t_attn += time.perf_counter() - t1
+        done_rows += n
+        done_flops += float(np.sum(lens[toks // w.block])) * 4.0 * w.block * D
+        n = min(n * 2, 65536)
+    total_rows = w.lanes * S
+    flops_all = visited_flops(int(rp[-1]), w.lanes, D, w.block)
+    attn_full_s = t_attn * (flops_all / done_flops)
+    step_s = t_build + attn_full_s
+    return {"value": round(flops_all / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"full schedule build ({t_build:.2f} s) + {done_rows} of {total_rows} attention "
+                       f"rows ({t_attn:.1f} s), attention extrapolated by visited FLOPs; "
+                       f"step estimate {step_s:.1f} s")}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle on this workload (rank 0 only)."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    topo = args.schedule == "topology"
+    q, k, v = make_qkv(w, seed=0, device="cpu")
+    if topo:
+        rp = ci = None
+    elif args.schedule == "dense":
+        import oracle
+        rp, ci = oracle.dense_causal_csr(w.nb)
+    else:
+        rp, ci = build_schedule_host(w, args.schedule)
+    # each step is a bounded sample, so that warm-up + steps stay within a few minutes
+    args.cpu_seconds = max(1.0, 150.0 / max(1, args.warmup + args.steps))
+    times, bl = [], None
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        bl = cpu_baseline(args, w, q, k, v, torch.as_tensor(rp) if rp is not None else None,
+                          torch.as_tensor(ci) if ci is not None else None, topo)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    line = {
+        "impl": "reference",
+        "metric": "scheduled-attn fwd TFLOP/s on visited blocks (% of GB300 bf16 peak); ms/call",
+        "value": bl["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded, same recipe as the GPU arm)",
+        "config": {"workload": f"{args.workload}: {w.describe()}", "schedule": args.schedule},
+        "ms_per_step_sample": round(1e3 * statistics.mean(times), 1),
+        "cpu_baseline": bl,
+        "e2e": {"value": bl["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,157 @@
+/*
+ * tsa.h -- C ABI of libtsa, topology-scheduled sparse attention for GB300 (sm_103a).
+ *
+ * Method: "Add topology-derived sparse attention kernel" (triton-lang/kernels#22),
+ * Summary; and the port note on that PR's GitHub mirror page ("A port of the Triton
+ * kernel merged as triton-lang/kernels#22").  Three operations:
+ *
+ *   tsa_build_schedule      -- causal CSR block schedule from K: sink blocks, local-window
+ *                              blocks and top-k blocks by 0D-persistence (elder-rule)
+ *                              salience over key-block centroids.
+ *   tsa_dense_causal_csr    -- the dense causal CSR (every block j <= i).
+ *   tsa_scheduled_attention -- forward causal attention that visits, for each 64-token query
+ *                              block, only the key blocks in its CSR row (online softmax,
+ *                              token-level causal mask in the diagonal block).
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument except `salience_sq` is required.  Buffers are DEVICE memory
+ *     of the current CUDA device, allocated and owned by the caller; the library never
+ *     allocates or frees and keeps no pointer after a call returns.
+ *   - Calls are asynchronous and stream-ordered on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  The return value reports only what the host can check
+ *     before launch.  Problems met on the device (an out-of-range or unsorted col_idx, a
+ *     wait that timed out) set a device status word read by tsa_last_device_status().
+ *     No kernel traps.
+ *   - Dense tensors are contiguous row-major.  A lane is one [S, D] matrix; [B, H, S, D]
+ *     input is B*H lanes stored back to back ([S, D] input is B = H = 1).  One CSR is
+ *     shared by all lanes.
+ *   - A CSR schedule is int32: row_ptr[nb + 1] with row_ptr[0] = 0 and non-decreasing,
+ *     col_idx[row_ptr[nb]]; row i lists key blocks j, strictly ascending, 0 <= j <= i.
+ *     nb = S / block.  The number of stored blocks (nnz) is row_ptr[nb], on the device.
+ */
+#ifndef TSA_H_
+#define TSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Stream handle: the same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *tsa_stream_t;
+
+typedef enum {
+    TSA_OK = 0,
+    TSA_ERR_INVALID_ARGUMENT = 1,  /* null pointer, non-positive size, S % block != 0, ...  */
+    TSA_ERR_UNSUPPORTED = 2,       /* valid request this build does not implement          */
+    TSA_ERR_NOT_DEVICE_POINTER = 3,/* a buffer is not device memory                        */
+    TSA_ERR_DEVICE_MISMATCH = 4,   /* a buffer lives on another device than the current one */
+    TSA_ERR_CAPACITY = 5,          /* col_cap or workspace_bytes too small                 */
+    TSA_ERR_CUDA = 6,              /* a CUDA runtime / driver call failed                  */
+    TSA_ERR_TIMEOUT = 7,           /* device: a bounded wait gave up (kernel returned)     */
+    TSA_ERR_BAD_SCHEDULE = 8,      /* device: a CSR row broke the contract above           */
+    TSA_ERR_DEVICE = 9             /* device: another device-side check failed             */
+} tsa_status;
+
+typedef enum { TSA_F16 = 0, TSA_BF16 = 1 } tsa_dtype;
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char *tsa_status_string(tsa_status status);
+
+/*
+ * Upper bound on the nnz of a topology schedule:
+ *   sum_{i=0}^{nb-1} min(i + 1, sink + local_radius + 1 + topk),  nb = S / block.
+ * Size col_idx with at least this many entries for tsa_build_schedule.
+ * Returns -1 for invalid arguments (S <= 0, block <= 0, S % block != 0, negative counts).
+ */
+int64_t tsa_schedule_max_nnz(int64_t S, int64_t block, int64_t sink, int64_t local_radius,
+                             int64_t topk);
+
+/*
+ * Bytes of device workspace tsa_build_schedule needs for `lanes` lanes of [S, D] keys
+ * (per-lane block sums, centroids, the pairwise distance matrix and MST state).
+ * Returns 0 for invalid arguments.
+ */
+size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, int64_t block);
+
+/*
+ * Topology schedule ("Add topology-derived sparse attention kernel", Summary: sink blocks,
+ * local-window blocks and a 0D-persistence-style salience over key-block centroids; the
+ * mirror page's port note: the salience is the elder rule and exactly one block scores 0).
+ *
+ *   K            [lanes, S, D] keys (f16 or bf16 per dtype).
+ *   centroids    C[b][d] = (sum_lanes (sum_{t in block b} K)) / (block * lanes), binary64,
+ *                both sums sequential in ascending order.
+ *   distance     d2(u,v) = sum_d (C[u][d] - C[v][d])^2, ascending d, fused multiply-add.
+ *   salience     Kruskal order on edges (d2, min(u,v), max(u,v)); the smaller component is
+ *                absorbed, on a size tie the one whose root has the larger index; the
+ *                absorbed root gets the edge's d2 (squared merge distance); one block keeps 0.
+ *   row i        {j < sink} U {max(0, i - local_radius) .. i} U {topk blocks j <= i of
+ *                largest salience, lower j on ties}, all clipped to j <= i, ascending.
+ *
+ *   row_ptr      out, nb + 1 int32.       col_idx  out, col_cap int32 (>= tsa_schedule_max_nnz).
+ *   salience_sq  out, nb binary64 (optional, may be NULL): per-block squared merge distance.
+ *   workspace    scratch of >= tsa_build_schedule_workspace_bytes(lanes, S, D, block) bytes,
+ *                256-byte aligned; its contents on entry do not matter.
+ *
+ * Limits: 1 <= block, S % block == 0, 1 <= nb <= 4096, 1 <= D <= 1024, lanes >= 1.
+ * Errors: INVALID_ARGUMENT, NOT_DEVICE_POINTER, DEVICE_MISMATCH, CAPACITY, UNSUPPORTED
+ * (nb or D beyond the limits), CUDA.  The result is bit-identical to the CPU oracle.
+ */
+tsa_status tsa_build_schedule(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S,
+                              int64_t D, int64_t block, int64_t sink, int64_t local_radius,
+                              int64_t topk, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                              double *salience_sq, void *workspace, size_t workspace_bytes,
+                              tsa_stream_t stream);
+
+/*
+ * Dense causal CSR ("Add topology-derived sparse attention kernel", Summary: "dense causal
+ * CSR layout"; Local benchmark: the dense CSR path visits every causal block):
+ * row_ptr[i] = i(i+1)/2, row i = 0..i.  nnz = nb(nb+1)/2 (136 at nb 16, 2080 at nb 64).
+ *
+ *   row_ptr out, nb + 1 int32;  col_idx out, col_cap >= nb(nb+1)/2 int32.
+ * Limits: S % block == 0, nb(nb+1)/2 < 2^31.  Errors: INVALID_ARGUMENT, CAPACITY,
+ * NOT_DEVICE_POINTER, DEVICE_MISMATCH, CUDA.
+ */
+tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int32_t *col_idx,
+                                int64_t col_cap, tsa_stream_t stream);
+
+/*
+ * Scheduled attention forward ("Add topology-derived sparse attention kernel", Summary:
+ * forward-only kernel over causal CSR block schedules, [seq, dim] and [batch, heads, seq,
+ * dim] inputs sharing one CSR, output in the input dtype; mirror page port note: running
+ * maximum and denominator, rescale by exp(m_prev - m_new)).
+ *
+ * For lane l and query token q of query block i = q / 64:
+ *   O[l][q] = sum_{k : k/64 in row i, k <= q} softmax_k(scale * <Q[l][q], K[l][k]>) V[l][k]
+ * accumulated in fp32 from f16/bf16 inputs and rounded to the input dtype.  A query with
+ * no allowed key gets O = 0.
+ *
+ *   Q, K, V  in,  [B*H, S, D] of `dtype`, 16-byte aligned.
+ *   O        out, same shape and dtype (must not alias Q, K or V).
+ *   row_ptr, col_idx  the CSR (nb = S / 64 rows), on the device.
+ *
+ * Limits: block == 64, D in {64, 128}, S % 64 == 0, B*H <= 65535, B*H*S < 2^31.
+ * Errors: INVALID_ARGUMENT, UNSUPPORTED (block or D), NOT_DEVICE_POINTER, DEVICE_MISMATCH,
+ * CUDA.  Device-side: BAD_SCHEDULE (a row is truncated at its first bad entry), TIMEOUT.
+ */
+tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
+                                   const int32_t *row_ptr, const int32_t *col_idx, void *O,
+                                   tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
+                                   int64_t block, float scale, tsa_stream_t stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device status word of the current
+ * device: TSA_OK, or the first of TIMEOUT, BAD_SCHEDULE, CAPACITY-on-device (reported as
+ * TSA_ERR_DEVICE) raised by any call since the last read.  TSA_ERR_CUDA if the
+ * synchronization itself fails.
+ */
+tsa_status tsa_last_device_status(tsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSA_H_ */

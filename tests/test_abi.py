@@ -1,0 +1,81 @@
+"""The C ABI library builds, loads and exports every entry point declared in include/tsa.h;
+host-side argument checks that need no GPU return the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import topology_scheduled_gb300 as tsa
+from topology_scheduled_gb300.binding import SIGNATURES
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "tsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    L = tsa.lib()
+    names = _declared()
+    assert len(names) == 7
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in SIGNATURES, n
+
+
+def test_status_strings():
+    L = tsa.lib()
+    for code, name in tsa.STATUS_NAMES.items():
+        assert L.tsa_status_string(code).decode() == name
+
+
+def test_max_nnz_closed_form():
+    # sum_i min(i+1, sink+r+1+topk): 70 at 16 blocks for (1,1,2), 150 at 32, 310 at 64
+    assert tsa.tsa_schedule_max_nnz(1024, 64, 1, 1, 2) == 70
+    assert tsa.tsa_schedule_max_nnz(2048, 64, 1, 1, 2) == 150
+    assert tsa.tsa_schedule_max_nnz(4096, 64, 1, 1, 2) == 310
+    assert tsa.tsa_schedule_max_nnz(8192, 64, 1, 2, 4) == 996
+    assert tsa.tsa_schedule_max_nnz(32768, 64, 2, 4, 8) == 7575
+    assert tsa.tsa_schedule_max_nnz(1024, 64, 0, 100, 0) == 136
+    assert tsa.tsa_schedule_max_nnz(1000, 64, 1, 1, 2) == -1
+    assert tsa.tsa_schedule_max_nnz(1024, 64, -1, 1, 2) == -1
+
+
+def test_workspace_bytes():
+    assert tsa.tsa_build_schedule_workspace_bytes(64, 32768, 128, 64) >= 64 * 512 * 128 * 8 + 512 * 512 * 8
+    assert tsa.tsa_build_schedule_workspace_bytes(1, 64 * 4097, 64, 64) == 0  # beyond 4096 blocks
+    assert tsa.tsa_build_schedule_workspace_bytes(1, 100, 64, 64) == 0
+
+
+def test_host_checks_before_any_device_call():
+    L = tsa.lib()
+    fake = ctypes.c_void_p(4096)
+    # null pointers
+    assert L.tsa_scheduled_attention(None, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 64, 0.1, None) == 1
+    assert L.tsa_build_schedule(None, 0, 1, 64, 64, 64, 1, 1, 2, fake, fake, 10, None, fake, 1 << 20, None) == 1
+    assert L.tsa_dense_causal_csr(64, 64, None, fake, 1, None) == 1
+    # unsupported block or head dimension
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 32, 0.1, None) == 2
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 96, 64, 0.1, None) == 2
+    # S not a multiple of the block, bad dtype, non-finite scale, misaligned pointer
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 100, 64, 64, 0.1, None) == 1
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 5, 1, 1, 64, 64, 64, 0.1, None) == 1
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 64,
+                                     float("nan"), None) == 1
+    odd = ctypes.c_void_p(4098)
+    assert L.tsa_scheduled_attention(odd, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 64, 0.1, None) == 1
+    # output aliasing an input
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 64, 0.1, None) == 1
+    # capacity checks
+    assert L.tsa_dense_causal_csr(1024, 64, fake, fake, 135, None) == 5
+    assert L.tsa_build_schedule(fake, 0, 1, 1024, 64, 64, 1, 1, 2, fake, fake, 69, None, fake, 1 << 30,
+                                None) == 5
+    assert L.tsa_build_schedule(fake, 0, 1, 1024, 64, 64, 1, 1, 2, fake, fake, 70, None, fake, 16,
+                                None) == 5
+    # builder limits
+    assert L.tsa_build_schedule(fake, 0, 1, 64 * 4097, 64, 64, 1, 1, 2, fake, fake, 1 << 30, None, fake,
+                                1 << 40, None) == 2

@@ -1,0 +1,140 @@
+"""GPU schedule builder vs the CPU oracle: bit-exact CSR and salience.
+
+Covers the dense causal CSR, the topology schedule on every workload shape (single lane,
+lane-mean over 64 lanes at S 8192 and S 32768), tiny and ragged inputs (D = 1, block = 1,
+one block, ties from duplicated blocks), the largest accepted block count, and the invariant
+that exactly one block has zero salience.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import topology_scheduled_gb300 as tsa
+from topology_scheduled_gb300.workloads import WORKLOADS, make_qkv
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _trim(rp, ci):
+    rp = rp.cpu().numpy()
+    return rp, ci.cpu().numpy()[: rp[-1]]
+
+
+def _gpu_schedule(K, block, sink, r, topk):
+    rp, ci, sal = tsa.tsa_build_schedule(K, block, sink, r, topk, salience=True)
+    assert tsa.tsa_last_device_status() == 0
+    rp, ci = _trim(rp, ci)
+    return rp, ci, sal.cpu().numpy()
+
+
+def _oracle_schedule(K, block, sink, r, topk):
+    S, D = K.shape[-2], K.shape[-1]
+    return oracle.build_schedule(K.detach().cpu().reshape(-1, S, D), block, sink, r, topk)
+
+
+def _assert_same(gpu, ref, distinct=True):
+    rp, ci, sal = gpu
+    rp_o, ci_o, sal_o = ref
+    assert np.array_equal(sal.view(np.uint64), sal_o.view(np.uint64)), "salience bits differ"
+    assert np.array_equal(rp, rp_o), "row_ptr differs"
+    assert np.array_equal(ci, ci_o), "col_idx differs"
+    # exactly one block is never absorbed; coincident centroids add zero-distance merges
+    assert int(np.sum(sal == 0)) == 1 if distinct else int(np.sum(sal == 0)) >= 1
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 16, 32, 64, 255, 512, 1025])
+def test_dense_csr_bit_exact(nb):
+    rp, ci = tsa.tsa_dense_causal_csr(nb * 64, 64)
+    rp_o, ci_o = oracle.dense_causal_csr(nb)
+    assert np.array_equal(rp.cpu().numpy(), rp_o)
+    assert np.array_equal(ci.cpu().numpy(), ci_o)
+    if nb in (16, 32, 64):
+        assert int(rp_o[-1]) == {16: 136, 32: 528, 64: 2080}[nb]
+
+
+@pytest.mark.parametrize("name", ["s1024", "s2048", "s4096"])
+def test_topology_single_lane_workloads(name):
+    w = WORKLOADS[name]
+    _, k, _ = make_qkv(w, seed=0, device=DEV)
+    gpu = _gpu_schedule(k, w.block, w.sink, w.local_radius, w.topk)
+    ref = _oracle_schedule(k, w.block, w.sink, w.local_radius, w.topk)
+    _assert_same(gpu, ref)
+    nnz = int(gpu[0][-1])
+    assert nnz <= tsa.tsa_schedule_max_nnz(w.S, w.block, w.sink, w.local_radius, w.topk)
+
+
+@pytest.mark.parametrize("name", ["b4h16s8192", "b2h32s32768"])
+def test_topology_lane_mean_workloads(name):
+    w = WORKLOADS[name]
+    _, k, _ = make_qkv(w, seed=0, device=DEV)
+    gpu = _gpu_schedule(k, w.block, w.sink, w.local_radius, w.topk)
+    ref = _oracle_schedule(k, w.block, w.sink, w.local_radius, w.topk)
+    _assert_same(gpu, ref)
+
+
+def _hand_cases():
+    rows = [l.split() for l in open("tests/golden/elder_rule_examples.txt") if l.strip() and not l.startswith("#")]
+    return [([float(x) for x in r[1:]], [float(x) for x in rows[i + 1][1:]])
+            for i, r in enumerate(rows) if r[0] == "points"]
+
+
+def test_hand_worked_elder_cases_on_gpu():
+    for points, sal in _hand_cases():
+        k = torch.tensor(points, dtype=torch.float16, device=DEV).view(1, -1, 1)
+        _, _, got = _gpu_schedule(k, 1, 0, 0, 0)
+        assert list(got) == sal
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_small_and_ragged(seed):
+    g = np.random.default_rng(seed)
+    lanes = int(g.integers(1, 5))
+    block = int(g.choice([1, 2, 8, 64]))
+    nb = int(g.integers(1, 70))
+    D = int(g.choice([1, 3, 8, 64, 128]))
+    dtype = torch.float16 if seed % 2 else torch.bfloat16
+    gen = torch.Generator().manual_seed(seed)
+    k = torch.randn((lanes, nb * block, D), generator=gen)
+    if seed % 3 == 0 and nb > 3:  # duplicated blocks force distance ties
+        k[:, block:2 * block] = k[:, 0:block]
+        k[:, 3 * block:4 * block] = k[:, 0:block]
+    if seed % 4 == 1:  # small integers: many exactly equal distances
+        k = torch.randint(-2, 3, k.shape, generator=gen).float()
+    k = k.to(dtype).to(DEV)
+    sink, r, topk = int(g.integers(0, 3)), int(g.integers(0, 4)), int(g.integers(0, 6))
+    _assert_same(_gpu_schedule(k, block, sink, r, topk), _oracle_schedule(k, block, sink, r, topk),
+                 distinct=(seed % 3 != 0 and seed % 4 != 1 and D * block > 2))
+
+
+def test_largest_block_count():
+    nb = 4096
+    gen = torch.Generator().manual_seed(7)
+    k = torch.randn((1, nb * 4, 16), generator=gen).to(torch.bfloat16).to(DEV)
+    _assert_same(_gpu_schedule(k, 4, 2, 3, 5), _oracle_schedule(k, 4, 2, 3, 5))
+
+
+def test_special_cases_reduce_to_dense_and_diagonal():
+    gen = torch.Generator().manual_seed(11)
+    k = torch.randn((2, 40 * 64, 64), generator=gen).to(torch.float16).to(DEV)
+    rp, ci, _ = _gpu_schedule(k, 64, 0, 39, 0)
+    rp_o, ci_o = oracle.dense_causal_csr(40)
+    assert np.array_equal(rp, rp_o) and np.array_equal(ci, ci_o)
+    rp, ci, _ = _gpu_schedule(k, 64, 0, 0, 0)
+    assert np.array_equal(rp, np.arange(41)) and np.array_equal(ci, np.arange(40))
+
+
+def test_host_errors_with_device_tensors():
+    k = torch.randn((1, 256, 64), device=DEV).to(torch.float16)
+    with pytest.raises(tsa.TsaError) as e:
+        tsa.tsa_build_schedule(k, 64, 1, 1, 2, col_idx=torch.empty(3, dtype=torch.int32, device=DEV))
+    assert e.value.status == 5
+    L = tsa.lib()
+    rp = torch.empty(5, dtype=torch.int32, device=DEV)
+    ci = torch.empty(10, dtype=torch.int32, device=DEV)
+    ws = torch.empty(tsa.tsa_build_schedule_workspace_bytes(1, 256, 64, 64), dtype=torch.uint8, device=DEV)
+    host_k = torch.randn((1, 256, 64)).to(torch.float16)
+    st = L.tsa_build_schedule(host_k.data_ptr(), 0, 1, 256, 64, 64, 1, 1, 2, rp.data_ptr(), ci.data_ptr(),
+                              10, None, ws.data_ptr(), ws.numel(), None)
+    assert st == 3

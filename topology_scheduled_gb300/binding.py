@@ -1,0 +1,192 @@
+"""Python binding of libtsa (include/tsa.h): argument marshalling only.
+
+Every step of the schedule builder and of the attention runs in the CUDA kernels of
+libtsa.so; PyTorch only provides device memory and the current stream.  There is no
+fallback: if the library is missing or a call fails, the functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+TSA_OK = 0
+STATUS_NAMES = {
+    0: "TSA_OK", 1: "TSA_ERR_INVALID_ARGUMENT", 2: "TSA_ERR_UNSUPPORTED",
+    3: "TSA_ERR_NOT_DEVICE_POINTER", 4: "TSA_ERR_DEVICE_MISMATCH", 5: "TSA_ERR_CAPACITY",
+    6: "TSA_ERR_CUDA", 7: "TSA_ERR_TIMEOUT", 8: "TSA_ERR_BAD_SCHEDULE", 9: "TSA_ERR_DEVICE",
+}
+TSA_F16, TSA_BF16 = 0, 1
+
+_LOCK = threading.Lock()
+_LIB = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes), mirroring include/tsa.h
+SIGNATURES = {
+    "tsa_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "tsa_schedule_max_nnz": (_I64, [_I64, _I64, _I64, _I64, _I64]),
+    "tsa_build_schedule_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
+    "tsa_build_schedule": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                          _P, _P, _I64, _P, _P, _SZ, _P]),
+    "tsa_dense_causal_csr": (ctypes.c_int, [_I64, _I64, _P, _P, _I64, _P]),
+    "tsa_scheduled_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
+                                               _I64, _I64, _I64, ctypes.c_float, _P]),
+    "tsa_last_device_status": (ctypes.c_int, [_P]),
+}
+
+
+class TsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """The loaded libtsa.so (built on first use when nvcc is available)."""
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            path = _build.LIB
+            if build_if_missing:
+                path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"libtsa.so is not built ({path}); run "
+                                   "`python -m topology_scheduled_gb300.build`")
+            L = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _LIB = L
+    return _LIB
+
+
+def _check(status: int, where: str):
+    if status != TSA_OK:
+        raise TsaError(status, where)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float16:
+        return TSA_F16
+    if t.dtype == torch.bfloat16:
+        return TSA_BF16
+    raise TypeError(f"expected float16 or bfloat16, got {t.dtype}")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _lanes_S_D(x: torch.Tensor):
+    if x.dim() == 2:
+        return 1, 1, x.shape[0], x.shape[1]
+    if x.dim() == 3:
+        return 1, x.shape[0], x.shape[1], x.shape[2]
+    if x.dim() == 4:
+        return x.shape[0], x.shape[1], x.shape[2], x.shape[3]
+    raise ValueError(f"expected [S, D], [L, S, D] or [B, H, S, D], got shape {tuple(x.shape)}")
+
+
+def tsa_schedule_max_nnz(S: int, block: int, sink: int, local_radius: int, topk: int) -> int:
+    return int(lib().tsa_schedule_max_nnz(S, block, sink, local_radius, topk))
+
+
+def tsa_build_schedule_workspace_bytes(lanes: int, S: int, D: int, block: int) -> int:
+    return int(lib().tsa_build_schedule_workspace_bytes(lanes, S, D, block))
+
+
+def tsa_build_schedule(K: torch.Tensor, block: int = 64, sink: int = 1, local_radius: int = 1,
+                       topk: int = 2, *, salience: bool = False, workspace: torch.Tensor | None = None,
+                       row_ptr: torch.Tensor | None = None, col_idx: torch.Tensor | None = None,
+                       stream=None):
+    """Topology CSR from K ([S, D], [L, S, D] or [B, H, S, D]; lane-mean centroids).
+
+    Returns (row_ptr, col_idx) int32 device tensors -- col_idx has capacity length, its first
+    row_ptr[-1] entries are the schedule -- plus the per-block squared merge distance (float64)
+    when ``salience`` is true.
+    """
+    if not K.is_cuda or not K.is_contiguous():
+        raise ValueError("K must be a contiguous CUDA tensor")
+    B, H, S, D = _lanes_S_D(K)
+    lanes = B * H
+    L = lib()
+    nb = S // block if block > 0 else 0
+    cap = int(L.tsa_schedule_max_nnz(S, block, sink, local_radius, topk))
+    if cap < 0:
+        raise TsaError(1, "tsa_schedule_max_nnz")
+    ws_bytes = int(L.tsa_build_schedule_workspace_bytes(lanes, S, D, block))
+    if ws_bytes == 0:
+        raise TsaError(2, "tsa_build_schedule_workspace_bytes")
+    dev = K.device
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if row_ptr is None:
+        row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+    if col_idx is None:
+        col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    sal = torch.empty(nb, dtype=torch.float64, device=dev) if salience else None
+    _check(L.tsa_build_schedule(K.data_ptr(), _dtype_code(K), lanes, S, D, block, sink,
+                                local_radius, topk, row_ptr.data_ptr(), col_idx.data_ptr(),
+                                col_idx.numel(), sal.data_ptr() if sal is not None else None,
+                                workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "tsa_build_schedule")
+    return (row_ptr, col_idx, sal) if salience else (row_ptr, col_idx)
+
+
+def tsa_dense_causal_csr(S: int, block: int = 64, device=None, stream=None):
+    """Dense causal CSR (row i = blocks 0..i) as int32 device tensors."""
+    nb = S // block if block > 0 else 0
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+    nnz = nb * (nb + 1) // 2
+    col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=dev)
+    _check(lib().tsa_dense_causal_csr(S, block, row_ptr.data_ptr(), col_idx.data_ptr(),
+                                      col_idx.numel(), _stream(stream)), "tsa_dense_causal_csr")
+    return row_ptr, col_idx[:nnz] if nnz > 0 else col_idx[:0]
+
+
+def tsa_scheduled_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+                            row_ptr: torch.Tensor, col_idx: torch.Tensor, scale: float | None = None,
+                            *, out: torch.Tensor | None = None, block: int = 64, stream=None):
+    """CSR-scheduled causal attention forward; output in the input dtype and shape."""
+    for name, t in (("Q", Q), ("K", K), ("V", V)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if not (Q.shape == K.shape == V.shape) or not (Q.dtype == K.dtype == V.dtype):
+        raise ValueError("Q, K, V must share shape and dtype")
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+        raise TypeError("row_ptr and col_idx must be int32 (the CSR schedule dtype)")
+    B, H, S, D = _lanes_S_D(Q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(Q)
+    elif out.shape != Q.shape or out.dtype != Q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor with Q's shape and dtype")
+    ci = col_idx if col_idx.numel() > 0 else torch.zeros(1, dtype=torch.int32, device=Q.device)
+    _check(lib().tsa_scheduled_attention(Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                         row_ptr.data_ptr(), ci.data_ptr(), out.data_ptr(),
+                                         _dtype_code(Q), B, H, S, D, block, float(scale),
+                                         _stream(stream)), "tsa_scheduled_attention")
+    return out
+
+
+def tsa_last_device_status(stream=None) -> int:
+    """Synchronizes the stream; returns and clears the device status word (0 = TSA_OK)."""
+    return int(lib().tsa_last_device_status(_stream(stream)))

@@ -1,0 +1,289 @@
+// api.cu -- the C ABI declared in include/tsa.h: host-side validation, tensor-map encoding
+// and kernel launches.  No call allocates or frees memory.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "tsa_internal.h"
+
+namespace tsa {
+namespace {
+
+__device__ unsigned g_status;       // sticky device-side error bits
+__device__ unsigned g_abort_epoch;  // epoch of the last launch that gave up
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+    bool ready = false;
+    unsigned *status = nullptr;
+    unsigned *abort_epoch = nullptr;
+};
+DeviceState g_devices[kMaxDevices];
+std::mutex g_mutex;
+std::atomic<unsigned> g_epoch{0};
+
+tsa_status current_device(int *dev) {
+    if (cudaGetDevice(dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TSA_ERR_CUDA;
+    }
+    return (*dev >= 0 && *dev < kMaxDevices) ? TSA_OK : TSA_ERR_UNSUPPORTED;
+}
+
+// Device addresses of the status words (looked up once per device) and a fresh epoch.
+tsa_status device_flags(int dev, DeviceFlags *f) {
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        DeviceState &d = g_devices[dev];
+        if (!d.ready) {
+            if (cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status) != cudaSuccess ||
+                cudaGetSymbolAddress(reinterpret_cast<void **>(&d.abort_epoch), g_abort_epoch) !=
+                    cudaSuccess) {
+                cudaGetLastError();
+                return TSA_ERR_CUDA;
+            }
+            d.ready = true;
+        }
+        f->status = d.status;
+        f->abort_epoch = d.abort_epoch;
+    }
+    unsigned e;
+    do {
+        e = ++g_epoch;
+    } while (e == 0u || e == ~0u);
+    f->epoch = e;
+    return TSA_OK;
+}
+
+tsa_status check_device_ptr(const void *p, int dev) {
+    if (p == nullptr) return TSA_ERR_INVALID_ARGUMENT;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return TSA_ERR_NOT_DEVICE_POINTER;
+    }
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return TSA_ERR_NOT_DEVICE_POINTER;
+    if (at.device != dev) return TSA_ERR_DEVICE_MISMATCH;
+    return TSA_OK;
+}
+
+#define TSA_TRY(expr)                       \
+    do {                                    \
+        const tsa_status s_ = (expr);       \
+        if (s_ != TSA_OK) return s_;        \
+    } while (0)
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            p = nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// Row-major [rows, cols] 16-bit matrix; boxes of 64 columns (128 B, 128-byte swizzle) x box_rows.
+bool encode_2d(CUtensorMap *map, const void *ptr, bool bf16, uint64_t rows, uint64_t cols,
+               uint32_t box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void *>(ptr), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+int64_t max_nnz_bound(int64_t nb, int64_t sink, int64_t r, int64_t topk) {
+    // sum_{i < nb} min(i + 1, per), per = sink + r + 1 + topk (saturating at nb)
+    int64_t per = nb;
+    if (sink < nb && r < nb && topk < nb) per = sink + r + 1 + topk;
+    if (per >= nb) return nb * (nb + 1) / 2;
+    return per * (per + 1) / 2 + (nb - per) * per;
+}
+
+}  // namespace
+}  // namespace tsa
+
+using namespace tsa;
+
+extern "C" {
+
+const char *tsa_status_string(tsa_status s) {
+    switch (s) {
+        case TSA_OK: return "TSA_OK";
+        case TSA_ERR_INVALID_ARGUMENT: return "TSA_ERR_INVALID_ARGUMENT";
+        case TSA_ERR_UNSUPPORTED: return "TSA_ERR_UNSUPPORTED";
+        case TSA_ERR_NOT_DEVICE_POINTER: return "TSA_ERR_NOT_DEVICE_POINTER";
+        case TSA_ERR_DEVICE_MISMATCH: return "TSA_ERR_DEVICE_MISMATCH";
+        case TSA_ERR_CAPACITY: return "TSA_ERR_CAPACITY";
+        case TSA_ERR_CUDA: return "TSA_ERR_CUDA";
+        case TSA_ERR_TIMEOUT: return "TSA_ERR_TIMEOUT";
+        case TSA_ERR_BAD_SCHEDULE: return "TSA_ERR_BAD_SCHEDULE";
+        case TSA_ERR_DEVICE: return "TSA_ERR_DEVICE";
+    }
+    return "TSA_ERR_UNKNOWN";
+}
+
+int64_t tsa_schedule_max_nnz(int64_t S, int64_t block, int64_t sink, int64_t local_radius,
+                             int64_t topk) {
+    if (S <= 0 || block <= 0 || S % block != 0 || sink < 0 || local_radius < 0 || topk < 0) return -1;
+    return max_nnz_bound(S / block, sink, local_radius, topk);
+}
+
+size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, int64_t block) {
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return 0;
+    const int64_t nb = S / block;
+    if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return 0;
+    return schedule_workspace_layout(lanes, nb, D).total;
+}
+
+tsa_status tsa_build_schedule(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S, int64_t D,
+                              int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
+                              int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                              double *salience_sq, void *workspace, size_t workspace_bytes,
+                              tsa_stream_t stream) {
+    if (!K || !row_ptr || !col_idx || !workspace) return TSA_ERR_INVALID_ARGUMENT;
+    if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (sink < 0 || local_radius < 0 || topk < 0) return TSA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(K) & 1u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = S / block;
+    if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
+    if (lanes > INT64_MAX / S / D) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t need = max_nnz_bound(nb, sink, local_radius, topk);
+    if (col_cap < need) return TSA_ERR_CAPACITY;
+    const ScheduleWorkspace ws = schedule_workspace_layout(lanes, nb, D);
+    if (workspace_bytes < ws.total) return TSA_ERR_CAPACITY;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    TSA_TRY(check_device_ptr(K, dev));
+    TSA_TRY(check_device_ptr(row_ptr, dev));
+    TSA_TRY(check_device_ptr(col_idx, dev));
+    TSA_TRY(check_device_ptr(workspace, dev));
+    if (salience_sq) TSA_TRY(check_device_ptr(salience_sq, dev));
+    ScheduleLaunch a;
+    a.K = static_cast<const uint16_t *>(K);
+    a.bf16 = dtype == TSA_BF16;
+    a.lanes = lanes;
+    a.S = S;
+    a.D = D;
+    a.block = block;
+    a.nb = nb;
+    a.sink = sink < nb ? sink : nb;
+    a.local_radius = local_radius < nb ? local_radius : nb;
+    a.topk = topk < nb ? topk : nb;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.col_cap = col_cap;
+    a.salience_sq = salience_sq;
+    a.workspace = static_cast<uint8_t *>(workspace);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    TSA_TRY(device_flags(dev, &a.flags));
+    return launch_build_schedule(a);
+}
+
+tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int32_t *col_idx,
+                                int64_t col_cap, tsa_stream_t stream) {
+    if (!row_ptr || !col_idx) return TSA_ERR_INVALID_ARGUMENT;
+    if (S <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = S / block;
+    if (nb > 65534) return TSA_ERR_INVALID_ARGUMENT;  // nb(nb+1)/2 must stay below 2^31
+    if (col_cap < nb * (nb + 1) / 2) return TSA_ERR_CAPACITY;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    TSA_TRY(check_device_ptr(row_ptr, dev));
+    TSA_TRY(check_device_ptr(col_idx, dev));
+    return launch_dense_causal_csr(nb, row_ptr, col_idx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
+                                   const int32_t *row_ptr, const int32_t *col_idx, void *O,
+                                   tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
+                                   int64_t block, float scale, tsa_stream_t stream) {
+    if (!Q || !K || !V || !row_ptr || !col_idx || !O) return TSA_ERR_INVALID_ARGUMENT;
+    if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
+    if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
+    if (block != 64 || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
+    if (S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
+    const int64_t lanes = B * H;
+    if (lanes * S >= (int64_t)INT_MAX) return TSA_ERR_UNSUPPORTED;
+    for (const void *p : {Q, K, V, static_cast<const void *>(O)})
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return TSA_ERR_INVALID_ARGUMENT;
+    const size_t bytes = (size_t)(lanes * S * D) * 2;
+    if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
+        return TSA_ERR_INVALID_ARGUMENT;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    for (const void *p : {Q, K, V, static_cast<const void *>(O), static_cast<const void *>(row_ptr),
+                          static_cast<const void *>(col_idx)})
+        TSA_TRY(check_device_ptr(p, dev));
+    const bool bf16 = dtype == TSA_BF16;
+    const uint64_t rows = (uint64_t)(lanes * S);
+    CUtensorMap tmQ, tmK, tmV, tmO;
+    if (!encode_2d(&tmQ, Q, bf16, rows, (uint64_t)D, 128) || !encode_2d(&tmK, K, bf16, rows, (uint64_t)D, 64) ||
+        !encode_2d(&tmV, V, bf16, rows, (uint64_t)D, 64) || !encode_2d(&tmO, O, bf16, rows, (uint64_t)D, 64))
+        return TSA_ERR_CUDA;
+    AttnLaunch a;
+    a.tmQ = &tmQ;
+    a.tmK = &tmK;
+    a.tmV = &tmV;
+    a.tmO = &tmO;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.nb = (int)(S / block);
+    a.S = (int)S;
+    a.D = (int)D;
+    a.lanes = (int)lanes;
+    a.bf16 = bf16;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    TSA_TRY(device_flags(dev, &a.flags));
+    return launch_scheduled_attention(a);
+}
+
+tsa_status tsa_last_device_status(tsa_stream_t stream) {
+    int dev;
+    TSA_TRY(current_device(&dev));
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TSA_ERR_CUDA;
+    }
+    unsigned bits = 0;
+    const unsigned zero = 0;
+    if (cudaMemcpyFromSymbol(&bits, g_status, sizeof(bits)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return TSA_ERR_CUDA;
+    }
+    if (bits & kDevTimeout) return TSA_ERR_TIMEOUT;
+    if (bits & kDevBadSchedule) return TSA_ERR_BAD_SCHEDULE;
+    if (bits) return TSA_ERR_DEVICE;
+    return TSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,643 @@
+// schedule.cu -- CSR block schedules on the GPU: the dense causal CSR and the topology
+// schedule (sink blocks, local window, top-k blocks by elder-rule salience over key-block
+// centroids).
+//
+// Method: "Add topology-derived sparse attention kernel" (triton-lang/kernels#22), Summary
+// (schedule from sink blocks, local-window blocks and a 0D-persistence-style salience over
+// key-block centroids; dense causal CSR layout); the PR's mirror page, port note (the
+// salience is the elder rule, exactly one block scores zero, a size tie is broken by index)
+// and the world-model commit's schedule.py bullet (the salience follows from MST edges alone).
+//
+// The result is bit-identical to the CPU oracle because every floating-point step is fixed:
+//   C[b][d]  = (sum over lanes of (sum over the block's tokens, ascending)) / (block * lanes)
+//   d2(u,v)  = fma-accumulated sum of (C[u][d] - C[v][d])^2 over ascending d
+//   ordering = strict key (d2, min(u,v), max(u,v)), so the MST is unique and Boruvka here
+//              selects the same tree as Kruskal in the oracle.
+//
+// Kernels, in stream order:
+//   centroid_partial   per (lane, block, d): sum of the block's tokens     (HBM stream of K)
+//   centroid_final     per (block, d): sum over lanes, divide               (small)
+//   pairwise_d2        nb x nb squared distances, tiles with u-tile <= v-tile (FP64 ALU)
+//   boruvka_*          ceil(log2 nb) rounds: per-vertex lightest edge (all CTAs), then one
+//                      CTA picks per-component edges, hooks and relabels
+//   elder_salience     one CTA: bitonic sort of the nb-1 MST edges, sequential union-find
+//   topk_csr           one CTA: salience order, per-row bitmaps, row counts, scan, fill
+#include <climits>
+
+#include "tsa_device.cuh"
+#include "tsa_internal.h"
+
+namespace tsa {
+namespace {
+
+constexpr uint64_t kInfBits = 0x7FF0000000000000ull;  // +inf as binary64 bits
+
+__device__ __forceinline__ double widen(uint16_t bits, bool bf16) {
+    if (bf16) return (double)__uint_as_float((uint32_t)bits << 16);
+    return (double)__half2float(__ushort_as_half(bits));
+}
+
+// ---------------------------------------------------------------- centroids
+// part[l][b][d] = sum_{t=0}^{block-1} K[l][b*block+t][d], t ascending; 8 d per thread.
+__global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
+                                      int64_t S, int64_t D, int64_t block, int64_t nb,
+                                      double *__restrict__ part) {
+    const int64_t groups = D / 8;
+    const int64_t total = lanes * nb * groups;
+    for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = w % groups;
+        const int64_t lb = w / groups;  // l * nb + b
+        const int64_t l = lb / nb, b = lb % nb;
+        const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
+        double acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0;
+        int64_t t = 0;
+        for (; t + 8 <= block; t += 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + (t + u) * D));
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += widen((uint16_t)(w4[i] & 0xFFFFu), bf16);
+                    acc[2 * i + 1] += widen((uint16_t)(w4[i] >> 16), bf16);
+                }
+            }
+        }
+        for (; t < block; ++t) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += widen((uint16_t)(w4[i] & 0xFFFFu), bf16);
+                acc[2 * i + 1] += widen((uint16_t)(w4[i] >> 16), bf16);
+            }
+        }
+        double *dst = part + lb * D + g * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = acc[i];
+    }
+}
+
+// Same sums, one d per thread (any D, any alignment).
+__global__ void centroid_partial_scalar(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
+                                        int64_t S, int64_t D, int64_t block, int64_t nb,
+                                        double *__restrict__ part) {
+    const int64_t total = lanes * nb * D;
+    for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t d = w % D;
+        const int64_t lb = w / D;
+        const int64_t l = lb / nb, b = lb % nb;
+        const uint16_t *src = K + (l * S + b * block) * D + d;
+        double acc = 0.0;
+        for (int64_t t = 0; t < block; ++t) acc += widen(__ldg(src + t * D), bf16);
+        part[w] = acc;
+    }
+}
+
+// C[b][d] = (sum_{l ascending} part[l][b][d]) / (block * lanes)
+__global__ void centroid_final(const double *__restrict__ part, int64_t lanes, int64_t nb,
+                               int64_t D, double denom, double *__restrict__ C) {
+    const int64_t n = nb * D;
+    for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        double total = 0.0;
+        for (int64_t l = 0; l < lanes; ++l) total += part[l * n + w];
+        C[w] = total / denom;
+    }
+}
+
+// ---------------------------------------------------------------- pairwise distances
+constexpr int kPdTile = 32;   // pairs per tile side
+constexpr int kPdChunk = 32;  // d values staged per step
+
+// D2[u][v] = D2[v][u] = sum_{d ascending} fma((C[u][d]-C[v][d]), same, acc); only tiles with
+// u-tile <= v-tile run; each thread computes a 2 x 2 block of pairs.
+__global__ void __launch_bounds__(256) pairwise_d2(const double *__restrict__ C, int64_t nb,
+                                                   int64_t D, double *__restrict__ D2) {
+    const int tu = blockIdx.y, tv = blockIdx.x;
+    if (tu > tv) return;
+    __shared__ double cu[kPdTile][kPdChunk + 1];
+    __shared__ double cv[kPdTile][kPdChunk + 1];
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int64_t u0 = (int64_t)tu * kPdTile, v0 = (int64_t)tv * kPdTile;
+    double acc[2][2] = {{0.0, 0.0}, {0.0, 0.0}};
+    for (int64_t d0 = 0; d0 < D; d0 += kPdChunk) {
+        for (int i = threadIdx.x; i < kPdTile * kPdChunk; i += 256) {
+            const int r = i / kPdChunk, c = i % kPdChunk;
+            const int64_t d = d0 + c;
+            cu[r][c] = (u0 + r < nb && d < D) ? C[(u0 + r) * D + d] : 0.0;
+            cv[r][c] = (v0 + r < nb && d < D) ? C[(v0 + r) * D + d] : 0.0;
+        }
+        __syncthreads();
+        const int dn = (int)((D - d0) < kPdChunk ? (D - d0) : kPdChunk);
+        for (int c = 0; c < dn; ++c) {
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const double delta = cu[ty * 2 + i][c] - cv[tx * 2 + k][c];
+                    acc[i][k] = fma(delta, delta, acc[i][k]);
+                }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int64_t u = u0 + ty * 2 + i, v = v0 + tx * 2 + k;
+            if (u < nb && v < nb) {
+                D2[u * nb + v] = acc[i][k];
+                D2[v * nb + u] = acc[i][k];
+            }
+        }
+}
+
+// ---------------------------------------------------------------- Boruvka MST
+struct EdgeKey {
+    double d;
+    int a, b;  // a < b
+};
+
+__device__ __forceinline__ bool key_less(double d1, int a1, int b1, double d2, int a2, int b2) {
+    if (d1 < d2) return true;
+    if (d1 > d2) return false;
+    if (a1 != a2) return a1 < a2;
+    return b1 < b2;
+}
+
+__global__ void boruvka_init(int *__restrict__ comp, int nb, int *__restrict__ counters) {
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < nb; v += gridDim.x * blockDim.x) comp[v] = v;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        counters[0] = nb;  // components
+        counters[1] = 0;   // MST edges recorded
+    }
+}
+
+// One warp per vertex v: the lightest edge from v to another component.
+__global__ void boruvka_vertex_min(const double *__restrict__ D2, const int *__restrict__ comp,
+                                   int nb, const int *__restrict__ counters,
+                                   double *__restrict__ vb_d, int *__restrict__ vb_u) {
+    if (counters[0] <= 1) return;
+    const int lane = threadIdx.x & 31;
+    const int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (v >= nb) return;
+    const int cv = comp[v];
+    double bd = __longlong_as_double((long long)kInfBits);
+    int ba = INT_MAX, bb = INT_MAX, bu = -1;
+    const double *row = D2 + (int64_t)v * nb;
+    for (int u = lane; u < nb; u += 32) {
+        if (comp[u] == cv) continue;
+        const double d = row[u];
+        const int a = u < v ? u : v, b = u < v ? v : u;
+        if (key_less(d, a, b, bd, ba, bb)) { bd = d; ba = a; bb = b; bu = u; }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const double od = __shfl_xor_sync(0xffffffffu, bd, off);
+        const int oa = __shfl_xor_sync(0xffffffffu, ba, off);
+        const int ob = __shfl_xor_sync(0xffffffffu, bb, off);
+        const int ou = __shfl_xor_sync(0xffffffffu, bu, off);
+        if (key_less(od, oa, ob, bd, ba, bb)) { bd = od; ba = oa; bb = ob; bu = ou; }
+    }
+    if (lane == 0) {
+        vb_d[v] = bd;
+        vb_u[v] = bu;
+    }
+}
+
+// One CTA: per component the lightest outgoing edge (min over its vertices), hook along it
+// (a mutual pair keeps the smaller label as root), record each chosen edge once, flatten by
+// pointer jumping and relabel.
+__global__ void __launch_bounds__(1024) boruvka_merge(int *__restrict__ comp, int nb,
+                                                      int *__restrict__ counters,
+                                                      const double *__restrict__ vb_d,
+                                                      const int *__restrict__ vb_u,
+                                                      double *__restrict__ mst_d,
+                                                      int *__restrict__ mst_u,
+                                                      int *__restrict__ mst_v) {
+    if (counters[0] <= 1) return;
+    extern __shared__ __align__(16) uint8_t sm[];
+    unsigned long long *cb_d = reinterpret_cast<unsigned long long *>(sm);
+    unsigned long long *cb_ab = cb_d + nb;
+    volatile int *par = reinterpret_cast<volatile int *>(cb_ab + nb);
+    __shared__ int s_roots, s_edges;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (tid == 0) { s_roots = 0; s_edges = counters[1]; }
+    for (int c = tid; c < nb; c += nt) {
+        cb_d[c] = kInfBits;
+        cb_ab[c] = ~0ull;
+    }
+    __syncthreads();
+    for (int v = tid; v < nb; v += nt)
+        atomicMin(&cb_d[comp[v]], (unsigned long long)__double_as_longlong(vb_d[v]));
+    __syncthreads();
+    for (int v = tid; v < nb; v += nt) {
+        const int c = comp[v];
+        if ((unsigned long long)__double_as_longlong(vb_d[v]) == cb_d[c] && vb_u[v] >= 0) {
+            const unsigned a = (unsigned)min(v, vb_u[v]), b = (unsigned)max(v, vb_u[v]);
+            atomicMin(&cb_ab[c], ((unsigned long long)a << 32) | b);
+        }
+    }
+    __syncthreads();
+    for (int c = tid; c < nb; c += nt) {
+        if (comp[c] != c) continue;
+        const unsigned long long ab = cb_ab[c];
+        if (ab == ~0ull) { par[c] = c; continue; }
+        const int a = (int)(ab >> 32), b = (int)(ab & 0xFFFFFFFFu);
+        const int other = comp[a] == c ? comp[b] : comp[a];
+        const bool mutual = cb_ab[other] == ab;
+        par[c] = (mutual && c < other) ? c : other;
+        if (!mutual || c < other) {
+            const int idx = atomicAdd(&s_edges, 1);
+            if (idx < nb - 1) {
+                mst_d[idx] = __longlong_as_double((long long)cb_d[c]);
+                mst_u[idx] = a;
+                mst_v[idx] = b;
+            }
+        }
+    }
+    __syncthreads();
+    for (int iter = 0; iter < 64; ++iter) {
+        int changed = 0;
+        for (int c = tid; c < nb; c += nt) {
+            if (comp[c] != c) continue;
+            const int p = par[c];
+            const int pp = par[p];
+            if (p != pp) { par[c] = pp; changed = 1; }
+        }
+        if (!__syncthreads_or(changed)) break;
+    }
+    for (int c = tid; c < nb; c += nt)
+        if (comp[c] == c && par[c] == c) atomicAdd(&s_roots, 1);
+    __syncthreads();
+    for (int v = tid; v < nb; v += nt) comp[v] = par[comp[v]];
+    __syncthreads();
+    if (tid == 0) {
+        counters[0] = s_roots;
+        counters[1] = s_edges;
+    }
+}
+
+// ---------------------------------------------------------------- elder rule
+// Sort 64-bit key pairs ascending (lexicographic on (k1, k2)); n is a power of two.
+__device__ void bitonic_sort_pairs(unsigned long long *k1, unsigned long long *k2, int n) {
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < n; i += blockDim.x) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool up = (i & size) == 0;
+                    const bool gt = k1[i] > k1[j] || (k1[i] == k1[j] && k2[i] > k2[j]);
+                    if (gt == up) {
+                        const unsigned long long t1 = k1[i], t2 = k2[i];
+                        k1[i] = k1[j]; k2[i] = k2[j];
+                        k1[j] = t1; k2[j] = t2;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Root of x with path halving (which never changes a root); -1 if more than `limit` hops,
+// which a forest never needs.
+__device__ __forceinline__ int dsu_find(volatile int *parent, int x, int limit) {
+    for (int hops = 0; parent[x] != x; ++hops) {
+        if (hops > limit) return -1;
+        const int g = parent[parent[x]];
+        parent[x] = g;
+        x = g;
+    }
+    return x;
+}
+
+// Kruskal order over the MST edges; the smaller component is absorbed (size tie: the root
+// with the larger index); the absorbed root receives the edge's d2; one block keeps 0.
+__global__ void __launch_bounds__(1024) elder_salience(int nb, const int *__restrict__ counters,
+                                                       const double *__restrict__ mst_d,
+                                                       const int *__restrict__ mst_u,
+                                                       const int *__restrict__ mst_v, int pow2,
+                                                       double *__restrict__ sal,
+                                                       DeviceFlags flags) {
+    extern __shared__ __align__(16) uint8_t sm[];
+    unsigned long long *kd = reinterpret_cast<unsigned long long *>(sm);
+    unsigned long long *kab = kd + pow2;
+    volatile int *parent = reinterpret_cast<volatile int *>(kab + pow2);
+    volatile int *size = parent + nb;
+    const int ne = nb - 1;
+    if (threadIdx.x == 0 && counters[1] != ne) raise_status(flags, kDevCapacity);
+    for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
+        if (i < ne) {
+            kd[i] = (unsigned long long)__double_as_longlong(mst_d[i]);
+            kab[i] = ((unsigned long long)(unsigned)mst_u[i] << 32) | (unsigned)mst_v[i];
+        } else {
+            kd[i] = ~0ull;
+            kab[i] = ~0ull;
+        }
+    }
+    for (int v = threadIdx.x; v < nb; v += blockDim.x) {
+        parent[v] = v;
+        size[v] = 1;
+        sal[v] = 0.0;
+    }
+    __syncthreads();
+    bitonic_sort_pairs(kd, kab, pow2);
+    if (threadIdx.x == 0) {
+        for (int e = 0; e < ne; ++e) {
+            const int a = (int)(kab[e] >> 32), b = (int)(kab[e] & 0xFFFFFFFFu);
+            if (a < 0 || a >= nb || b < 0 || b >= nb) { raise_status(flags, kDevCapacity); break; }
+            const int ra = dsu_find(parent, a, nb), rb = dsu_find(parent, b, nb);
+            if (ra < 0 || rb < 0) { raise_status(flags, kDevCapacity); break; }
+            if (ra == rb) continue;
+            const int sa = size[ra], sb = size[rb];
+            int absorbed, survivor;
+            if (sa < sb) { absorbed = ra; survivor = rb; }
+            else if (sb < sa) { absorbed = rb; survivor = ra; }
+            else { absorbed = ra > rb ? ra : rb; survivor = ra > rb ? rb : ra; }
+            sal[absorbed] = __longlong_as_double((long long)kd[e]);
+            parent[absorbed] = survivor;
+            size[survivor] = sa + sb;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- top-k + CSR
+// Row i: {j < sink} U {max(0,i-r)..i} U {topk blocks j <= i by (salience desc, j asc)}.
+struct TopkSmem {
+    unsigned long long *ok1, *ok2;  // sort keys: ~salience bits, j
+    int *order;                     // blocks by (salience desc, j asc)
+    int *cnt;                       // per-row counts, then row starts
+    unsigned *bm;                   // one bitmap of `words` words per warp
+};
+
+__device__ void row_bitmap(const TopkSmem &s, unsigned *bm, int words, int nb, int i, int sink,
+                           int r, int topk) {
+    const int lane = threadIdx.x & 31;
+    const int s_end = min(sink, i + 1);           // sink blocks [0, s_end)
+    const int l_beg = max(0, i - r);              // local blocks [l_beg, i]
+    for (int w = lane; w < words; w += 32) {
+        const int lo = w * 32;
+        unsigned m = 0;
+        // bits [lo, lo+32) intersected with [0, s_end)
+        if (s_end > lo) m |= (s_end - lo >= 32) ? 0xFFFFFFFFu : ((1u << (s_end - lo)) - 1u);
+        // intersected with [l_beg, i]
+        const int a = max(l_beg, lo), b = min(i, lo + 31);
+        if (a <= b) {
+            const int n = b - a + 1;
+            const unsigned run = (n >= 32) ? 0xFFFFFFFFu : ((1u << n) - 1u);
+            m |= run << (a - lo);
+        }
+        bm[w] = m;
+    }
+    __syncwarp();
+    int need = min(topk, i + 1);
+    for (int base = 0; need > 0 && base < nb; base += 32) {
+        const int t = base + lane;
+        const int j = t < nb ? s.order[t] : INT_MAX;
+        const bool pred = j <= i;
+        const unsigned bal = __ballot_sync(0xffffffffu, pred);
+        const int rank = __popc(bal & ((1u << lane) - 1u));
+        if (pred && rank < need) atomicOr(&bm[j >> 5], 1u << (j & 31));
+        need -= __popc(bal);
+    }
+    __syncwarp();
+}
+
+__global__ void __launch_bounds__(1024) topk_csr(const double *__restrict__ sal, int nb, int pow2,
+                                                 int sink, int r, int topk,
+                                                 int32_t *__restrict__ row_ptr,
+                                                 int32_t *__restrict__ col_idx, int64_t col_cap,
+                                                 DeviceFlags flags) {
+    extern __shared__ __align__(16) uint8_t sm[];
+    const int words = (nb + 31) / 32;
+    const int nwarps = blockDim.x >> 5;
+    TopkSmem s;
+    s.ok1 = reinterpret_cast<unsigned long long *>(sm);
+    s.ok2 = s.ok1 + pow2;
+    s.order = reinterpret_cast<int *>(s.ok2 + pow2);
+    s.cnt = s.order + pow2;
+    s.bm = reinterpret_cast<unsigned *>(s.cnt + nb + 1);
+    __shared__ int warp_tot[32];
+    __shared__ int s_total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < pow2; i += blockDim.x) {
+        if (i < nb) {
+            s.ok1[i] = ~(unsigned long long)__double_as_longlong(sal[i]);  // salience >= 0
+            s.ok2[i] = (unsigned long long)i;
+        } else {
+            s.ok1[i] = ~0ull;
+            s.ok2[i] = ~0ull;
+        }
+    }
+    __syncthreads();
+    bitonic_sort_pairs(s.ok1, s.ok2, pow2);
+    for (int i = tid; i < nb; i += blockDim.x) s.order[i] = (int)s.ok2[i];
+    __syncthreads();
+    unsigned *bm = s.bm + warp * words;
+    // counts
+    for (int i = warp; i < nb; i += nwarps) {
+        row_bitmap(s, bm, words, nb, i, sink, r, topk);
+        int c = 0;
+        for (int w = lane; w < words; w += 32) c += __popc(bm[w]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
+        if (lane == 0) s.cnt[i] = c;
+        __syncwarp();
+    }
+    __syncthreads();
+    // exclusive scan of the counts (each thread a contiguous run)
+    const int per = (nb + blockDim.x - 1) / blockDim.x;
+    const int beg = min(nb, tid * per), end = min(nb, beg + per);
+    int run = 0;
+    for (int i = beg; i < end; ++i) run += s.cnt[i];
+    int incl = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += o;
+        }
+        warp_tot[lane] = t;  // inclusive over warps
+        if (lane == 31) s_total = t;
+    }
+    __syncthreads();
+    int start = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - run;
+    __syncthreads();
+    for (int i = beg; i < end; ++i) {
+        const int c = s.cnt[i];
+        s.cnt[i] = start;
+        row_ptr[i] = start;
+        start += c;
+    }
+    if (tid == 0) row_ptr[nb] = s_total;
+    __syncthreads();
+    if ((int64_t)s_total > col_cap) {
+        if (tid == 0) raise_status(flags, kDevCapacity);
+        return;
+    }
+    // fill
+    for (int i = warp; i < nb; i += nwarps) {
+        row_bitmap(s, bm, words, nb, i, sink, r, topk);
+        int off = s.cnt[i];
+        for (int w0 = 0; w0 < words; w0 += 32) {
+            const int w = w0 + lane;
+            unsigned bits = w < words ? bm[w] : 0u;
+            const int c = __popc(bits);
+            int inc = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int x = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += x;
+            }
+            int pos = off + inc - c;
+            while (bits) {
+                const int bit = __ffs(bits) - 1;
+                col_idx[pos++] = w * 32 + bit;
+                bits &= bits - 1u;
+            }
+            off += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------- dense causal CSR
+__global__ void dense_csr(int64_t nb, int32_t *__restrict__ row_ptr, int32_t *__restrict__ col_idx) {
+    const int64_t nnz = nb * (nb + 1) / 2;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i <= nb; i += stride)
+        row_ptr[i] = (int32_t)(i * (i + 1) / 2);
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < nnz; e += stride) {
+        int64_t i = (int64_t)((sqrt(8.0 * (double)e + 1.0) - 1.0) * 0.5);
+        while (i * (i + 1) / 2 > e) --i;
+        while ((i + 1) * (i + 2) / 2 <= e) ++i;
+        col_idx[e] = (int32_t)(e - i * (i + 1) / 2);
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int next_pow2(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+template <typename K>
+bool set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+           cudaSuccess;
+}
+
+}  // namespace
+
+ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D) {
+    ScheduleWorkspace w{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align256(o + bytes);
+        return at;
+    };
+    w.part = take(sizeof(double) * (size_t)(lanes * nb * D));
+    w.cent = take(sizeof(double) * (size_t)(nb * D));
+    w.d2 = take(sizeof(double) * (size_t)(nb * nb));
+    w.comp = take(sizeof(int) * (size_t)nb);
+    w.vb_d = take(sizeof(double) * (size_t)nb);
+    w.vb_u = take(sizeof(int) * (size_t)nb);
+    w.mst_d = take(sizeof(double) * (size_t)nb);
+    w.mst_u = take(sizeof(int) * (size_t)nb);
+    w.mst_v = take(sizeof(int) * (size_t)nb);
+    w.counters = take(sizeof(int) * 4);
+    w.sal = take(sizeof(double) * (size_t)nb);
+    w.total = o;
+    return w;
+}
+
+tsa_status launch_build_schedule(const ScheduleLaunch &a) {
+    const int nb = (int)a.nb;
+    const ScheduleWorkspace ws = schedule_workspace_layout(a.lanes, a.nb, a.D);
+    uint8_t *w = a.workspace;
+    double *part = reinterpret_cast<double *>(w + ws.part);
+    double *cent = reinterpret_cast<double *>(w + ws.cent);
+    double *d2 = reinterpret_cast<double *>(w + ws.d2);
+    int *comp = reinterpret_cast<int *>(w + ws.comp);
+    double *vb_d = reinterpret_cast<double *>(w + ws.vb_d);
+    int *vb_u = reinterpret_cast<int *>(w + ws.vb_u);
+    double *mst_d = reinterpret_cast<double *>(w + ws.mst_d);
+    int *mst_u = reinterpret_cast<int *>(w + ws.mst_u);
+    int *mst_v = reinterpret_cast<int *>(w + ws.mst_v);
+    int *counters = reinterpret_cast<int *>(w + ws.counters);
+    double *sal = a.salience_sq ? a.salience_sq : reinterpret_cast<double *>(w + ws.sal);
+    cudaStream_t st = a.stream;
+
+    // centroids
+    const bool vec = (a.D % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.K) & 15u) == 0);
+    const int64_t items = vec ? a.lanes * a.nb * (a.D / 8) : a.lanes * a.nb * a.D;
+    const int threads = 256;
+    const int64_t blocks = (items + threads - 1) / threads;
+    const unsigned grid = (unsigned)(blocks < 152 * 64 ? blocks : 152 * 64);
+    if (vec)
+        centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb, part);
+    else
+        centroid_partial_scalar<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb, part);
+    {
+        const int64_t n = a.nb * a.D;
+        const unsigned g = (unsigned)((n + 255) / 256);
+        centroid_final<<<g, 256, 0, st>>>(part, a.lanes, a.nb, a.D, (double)(a.block * a.lanes), cent);
+    }
+    // distances
+    {
+        const unsigned t = (unsigned)((nb + kPdTile - 1) / kPdTile);
+        pairwise_d2<<<dim3(t, t), 256, 0, st>>>(cent, a.nb, a.D, d2);
+    }
+    // Boruvka MST
+    boruvka_init<<<(nb + 255) / 256, 256, 0, st>>>(comp, nb, counters);
+    int rounds = 0;
+    while ((1 << rounds) < nb) ++rounds;
+    const size_t merge_smem = (size_t)nb * (8 + 8 + 4);
+    const bool merge_ok = set_smem(boruvka_merge, 96 * 1024);
+    const int pow2 = next_pow2(nb);
+    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 8;
+    const bool elder_ok = set_smem(elder_salience, 160 * 1024);
+    const int words = (nb + 31) / 32;
+    const size_t topk_smem = (size_t)pow2 * 16 + (size_t)pow2 * 4 + (size_t)(nb + 1) * 4 + (size_t)32 * words * 4;
+    const bool topk_ok = set_smem(topk_csr, 200 * 1024);
+    if (!merge_ok || !elder_ok || !topk_ok) return TSA_ERR_CUDA;
+    for (int r = 0; r < rounds; ++r) {
+        boruvka_vertex_min<<<(nb + 7) / 8, 256, 0, st>>>(d2, comp, nb, counters, vb_d, vb_u);
+        boruvka_merge<<<1, 1024, merge_smem, st>>>(comp, nb, counters, vb_d, vb_u, mst_d, mst_u, mst_v);
+    }
+    // elder-rule salience, then the CSR
+    elder_salience<<<1, 1024, elder_smem, st>>>(nb, counters, mst_d, mst_u, mst_v, pow2, sal, a.flags);
+    topk_csr<<<1, 1024, topk_smem, st>>>(sal, nb, pow2, (int)a.sink, (int)a.local_radius, (int)a.topk,
+                                         a.row_ptr, a.col_idx, a.col_cap, a.flags);
+    return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
+}
+
+tsa_status launch_dense_causal_csr(int64_t nb, int32_t *row_ptr, int32_t *col_idx,
+                                   cudaStream_t stream) {
+    const int64_t nnz = nb * (nb + 1) / 2;
+    const int64_t n = nnz > nb + 1 ? nnz : nb + 1;
+    const int64_t blocks = (n + 255) / 256;
+    dense_csr<<<(unsigned)(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, stream>>>(nb, row_ptr, col_idx);
+    return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
+}
+
+}  // namespace tsa

@@ -1,0 +1,61 @@
+// tsa_internal.h -- declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "tsa.h"
+#include "tsa_device.cuh"
+
+namespace tsa {
+
+// Dynamic shared memory of the attention kernel.  The D = 128 figure is the largest size at
+// which two CTAs fit on one SM (2 x (115712 + 1024 reserved) = 228 KB); it covers the
+// 114816 bytes of tiles and barriers plus 896 bytes of alignment slack.
+template <int D>
+__host__ __device__ constexpr int kAttnSmemBytes() {
+    return D == 128 ? 115712 : 66688;
+}
+
+struct AttnLaunch {
+    const CUtensorMap *tmQ, *tmK, *tmV, *tmO;
+    const int32_t *row_ptr, *col_idx;
+    int nb, S, D, lanes;
+    bool bf16;
+    float scale_log2;
+    DeviceFlags flags;
+    cudaStream_t stream;
+};
+
+tsa_status launch_scheduled_attention(const AttnLaunch &a);
+
+// Largest number of blocks the schedule builder accepts.
+constexpr int64_t kMaxScheduleBlocks = 4096;
+constexpr int64_t kMaxScheduleDim = 1024;
+
+// Byte offsets of the builder's workspace regions (each 256-byte aligned).
+struct ScheduleWorkspace {
+    size_t part, cent, d2, comp, vb_d, vb_u, mst_d, mst_u, mst_v, counters, sal, total;
+};
+ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D);
+
+struct ScheduleLaunch {
+    const uint16_t *K;
+    bool bf16;
+    int64_t lanes, S, D, block, nb;
+    int64_t sink, local_radius, topk;
+    int32_t *row_ptr, *col_idx;
+    int64_t col_cap;
+    double *salience_sq;  // may be null
+    uint8_t *workspace;
+    DeviceFlags flags;
+    cudaStream_t stream;
+};
+
+tsa_status launch_build_schedule(const ScheduleLaunch &a);
+tsa_status launch_dense_causal_csr(int64_t nb, int32_t *row_ptr, int32_t *col_idx,
+                                   cudaStream_t stream);
+
+}  // namespace tsa
