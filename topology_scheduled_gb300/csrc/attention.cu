@@ -239,6 +239,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         const uint32_t sw = (uint32_t)(tid & 7);
         if (in_row) {
             uint32_t sr[2][32];
+            __syncwarp();  // the waits above may leave the warp diverged; tcgen05.ld is collective
             tmem_ld32(tmem + t_lane + L::kSCol, sr[0]);
             tmem_ld32(tmem + t_lane + L::kSCol + 32, sr[1]);
             const bool diag = (j == my_block);
@@ -251,9 +252,13 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 x[c] = v;
                 mx = fmaxf(mx, v);
             }
-            if (mx > m_used + kRescaleLog2) {
-                const float alpha = (m_used == -INFINITY) ? 0.f : ex2_approx(m_used - mx);
+            // The rescale decision is per row, but tcgen05.ld/st are warp-collective: the whole
+            // warp rescales when any of its rows must, with factor 1 for the other rows.
+            const bool grow = mx > m_used + kRescaleLog2;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : ex2_approx(m_used - mx));
                 if (o_valid) {
+                    __syncwarp();
 #pragma unroll
                     for (int c = 0; c < D; c += 32) {
                         uint32_t o[32];
@@ -263,8 +268,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         tmem_st32(tmem + t_lane + L::kOCol + c, o);
                     }
                 }
-                l_sum *= alpha;
-                m_used = mx;
+                if (grow) {
+                    l_sum *= alpha;
+                    m_used = mx;
+                }
             }
             float lsum_blk = 0.f;
 #pragma unroll
@@ -319,6 +326,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         // ---- epilogue: O / l in the input dtype, staged in the Q tile, TMA store per block
         const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
         const uint32_t sw = (uint32_t)(tid & 7);
+        __syncwarp();
 #pragma unroll
         for (int c = 0; c < L::kChunks; ++c) {
             const uint32_t o_row = sQ + c * 16384 + tid * 128;
