@@ -42,13 +42,15 @@ ATTN_SOURCE = os.path.join(ROOT, "topology_scheduled_gb300", "csrc", "attention.
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["tsa", "reference"], default="tsa")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     p.add_argument("--schedule", default="topology")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--heads", type=int, default=0,
+                   help="override H (a smaller case of the same workload, e.g. for ncu captures)")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle's attention sample")
     return p.parse_args()
@@ -95,7 +97,7 @@ def attention_traffic_per_launch(workload: str, schedule: str):
 class ClockSampler:
     """nvidia-smi clock / throttle samples during the timed region."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -112,7 +114,8 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t_begin: float, t_end: float):
+        """Summary of the samples taken between host times t_begin and t_end (time.time())."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -121,16 +124,37 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
-        if not rows:
-            return None
-        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        import datetime
+        rows = []
+        for r in csv.reader(io.StringIO(out)):
+            if len(r) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, [x.strip() for x in r[1:]]))
+        inside = [r for ts, r in rows if t_begin <= ts <= t_end]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        num = lambda x: float(x) if x.replace(".", "").isdigit() else None  # noqa: E731
+        sm = [num(r[1]) for r in inside if num(r[1]) is not None]
+        smax = [num(r[2]) for r in inside if num(r[2]) is not None]
+        power = [num(r[3]) for r in inside if num(r[3]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[5 + i] == "Active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
-                "reasons": reasons, "samples": len(rows)}
+                "power_w_max": max(power) if power else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+def workload(args):
+    w = WORKLOADS[args.workload]
+    if args.heads:
+        from dataclasses import replace
+        w = replace(w, H=args.heads, name=f"{w.name}-h{args.heads}")
+    return w
 
 
 def build_schedule_host(w, schedule: str):
@@ -152,7 +176,7 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = WORKLOADS[args.workload]
+    w = workload(args)
     stream = torch.cuda.current_stream()
     q, k, v = make_qkv(w, seed=rank, device=dev)
     out = torch.empty_like(q)
@@ -206,15 +230,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     t0, t1 = ev(), ev()
     wall0 = time.perf_counter()
+    host0 = time.time()
     t0.record(stream)
     for i in range(args.steps):
         step(attn_ev[i], build_ev[i])
     t1.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    host1 = time.time()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
+    clk = clocks.stop(host0, host1)
     status = tsa.tsa_last_device_status()
     if status != 0:
         raise RuntimeError(f"device status after timing {tsa.STATUS_NAMES.get(status, status)}")
@@ -258,7 +284,7 @@ def run_gpu(args):
         "dtype": dtype_name(w.dtype),
         "data": "synthetic (seeded N(0,1) Q/V, clustered K; no dataset)",
         "config": {
-            "workload": f"{args.workload}: {w.describe()}",
+            "workload": f"{w.name}: {w.describe()}",
             "schedule": args.schedule,
             "B": w.B, "H": w.H, "S": w.S, "D": w.D, "block": w.block,
             "nnz_blocks": nnz, "dense_blocks": w.nb * (w.nb + 1) // 2,
@@ -374,7 +400,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    w = WORKLOADS[args.workload]
+    w = workload(args)
     topo = args.schedule == "topology"
     q, k, v = make_qkv(w, seed=0, device="cpu")
     if topo:
@@ -385,7 +411,7 @@ def run_reference(args):
     else:
         rp, ci = build_schedule_host(w, args.schedule)
     # each step is a bounded sample, so that warm-up + steps stay within a few minutes
-    args.cpu_seconds = max(1.0, 150.0 / max(1, args.warmup + args.steps))
+    args.cpu_seconds = 120.0 / max(1, args.warmup + args.steps)
     times, bl = [], None
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
