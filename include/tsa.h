@@ -142,6 +142,37 @@ tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
                                    tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
                                    int64_t block, float scale, tsa_stream_t stream);
 
+/* Size of the device array behind tsa_build_schedule_noalloc: 16 MiB on every device that
+ * loads the library, held until the process exits. */
+#define TSA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * tsa_build_schedule for callers that cannot allocate device memory.  Some callers own no
+ * device allocator: a plugin running inside a host application that has already reserved the
+ * device memory for its own pool, or a latency-bound loop in which cudaMalloc's implicit
+ * device-wide synchronization is not acceptable.  This entry point takes no workspace; it
+ * uses a fixed scratch array of TSA_NOALLOC_SCRATCH_BYTES inside the library instead and
+ * calls no allocating routine.  The paper has no counterpart: this is a packaging choice of
+ * this library, not part of the method.
+ *
+ * Arguments, results and limits are those of tsa_build_schedule without `workspace` and
+ * `workspace_bytes`.  The scratch needed is tsa_build_schedule_workspace_bytes(lanes, S, D,
+ * block); above TSA_NOALLOC_SCRATCH_BYTES the call returns TSA_ERR_CAPACITY without launching
+ * anything (for example 64 lanes of [32768, 128] keys need about 35 MiB and are rejected,
+ * 64 lanes of [8192, 64] need about 4.2 MiB and fit).
+ *
+ * The first call on each device looks up the scratch array's device address (with that
+ * device current) and caches it; make that first call before any stream capture.  All calls
+ * on a device share the one array: calls that can overlap on the GPU (on different streams
+ * without ordering between them) race on it and must be serialized by the caller.  Nothing
+ * in the array needs to start at zero; a call never reads what an earlier call left there.
+ */
+tsa_status tsa_build_schedule_noalloc(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S,
+                                      int64_t D, int64_t block, int64_t sink,
+                                      int64_t local_radius, int64_t topk, int32_t *row_ptr,
+                                      int32_t *col_idx, int64_t col_cap, double *salience_sq,
+                                      tsa_stream_t stream);
+
 /*
  * Synchronizes `stream`, then returns and clears the device status word of the current
  * device: TSA_OK, or the first of TIMEOUT, BAD_SCHEDULE, CAPACITY-on-device (reported as

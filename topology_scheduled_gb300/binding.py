@@ -37,6 +37,8 @@ SIGNATURES = {
     "tsa_build_schedule_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "tsa_build_schedule": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
                                           _P, _P, _I64, _P, _P, _SZ, _P]),
+    "tsa_build_schedule_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64,
+                                                  _I64, _P, _P, _I64, _P, _P]),
     "tsa_dense_causal_csr": (ctypes.c_int, [_I64, _I64, _P, _P, _I64, _P]),
     "tsa_scheduled_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
                                                _I64, _I64, _I64, ctypes.c_float, _P]),
