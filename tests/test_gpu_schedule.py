@@ -138,3 +138,18 @@ def test_host_errors_with_device_tensors():
     st = L.tsa_build_schedule(host_k.data_ptr(), 0, 1, 256, 64, 64, 1, 1, 2, rp.data_ptr(), ci.data_ptr(),
                               10, None, ws.data_ptr(), ws.numel(), None)
     assert st == 3
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_centroid_sums_with_extreme_exponents(dtype):
+    """Keys spread over ~75 binades (subnormals, values outside the integer window, widely
+    spread columns): the block sums must still equal the sequential binary64 sums."""
+    g = torch.Generator().manual_seed(5)
+    lanes, nb, D = 3, 24, 64
+    x = torch.randn((lanes, nb * 64, D), generator=g)
+    hi = 30 if dtype == torch.bfloat16 else 13
+    e = torch.randint(-45, hi, x.shape, generator=g).float()
+    x = x * torch.pow(2.0, e)
+    x[:, :64, :8] = 1e-30  # columns of tiny values only (f16: zero, bf16: below the window)
+    k = x.to(dtype).to(DEV)
+    _assert_same(_gpu_schedule(k, 64, 1, 2, 3), _oracle_schedule(k, 64, 1, 2, 3), distinct=False)

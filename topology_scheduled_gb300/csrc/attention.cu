@@ -6,20 +6,27 @@
 // exp(m_prev - m_new), and mask keys after the query token inside the diagonal block.
 //
 // GB300 design (not the pages' Triton kernel):
-//  * One CTA computes a 128-row tile made of the query blocks 2p and 2p+1 of one lane, because
-//    tcgen05 reaches full rate at M = 128.  It walks the sorted union of the two CSR rows; a
-//    key block that is in only one row is masked for the other half (both halves are
-//    warp-uniform, so that half skips its softmax).
-//  * TMA loads Q once and K/V tiles per visited block (128-byte swizzle, two stages).  One
-//    thread issues S = Q K^T (M128 N64) into TMEM; 128 threads own one row each, read S with
-//    tcgen05.ld, do the online softmax in fp32 (exp2 with the scale folded in), write P in the
-//    input dtype to shared memory, and one thread issues O += P V (M128 N=D) into TMEM.
-//  * Rescaling is lazy: O and the denominator are rescaled only when a row's maximum grows by
-//    more than 2^8; the final O / l uses the same stale maximum, so the result is unchanged.
-//  * Epilogue: O / l rounded to the input dtype, staged in shared memory, TMA-stored per
-//    64-row block.
-//  * Two CTAs share an SM (D = 128; three for D = 64), so one CTA's softmax overlaps the
-//    other's MMAs.
+//  * Tile.  One CTA computes 128 query rows: query blocks 2p and 2p+1 of one lane, because
+//    tcgen05 runs at full rate at M = 128.  It walks the sorted union of the two CSR rows; a
+//    key block in only one row is masked for the other half (each half is two whole warps).
+//  * Warp roles (192 threads).  Warp 4 produces: TMA loads of Q once and of the K/V tiles of
+//    each visited block into a two-stage ring (128-byte swizzle).  Warp 5 issues the MMAs from
+//    one thread: S = Q K^T (M128 N64 K=D, both operands in shared memory) into one of two TMEM
+//    S buffers, and O += P V (M128 N=D K64) with P read from TMEM.  Warps 0-3 run the online
+//    softmax, one row per thread: tcgen05.ld of the S row, exp2 with the scale folded in, the
+//    new P written back over the S buffer in the input dtype with tcgen05.st.
+//  * Pipeline.  The MMA warp issues QK(u+1) before PV(u), so the tensor core computes the next
+//    scores while the softmax warps work on the current ones.  Hand-offs are mbarriers:
+//    kv_full/kv_empty (producer <-> MMA), s_full (MMA -> softmax), p_full (softmax -> MMA),
+//    o_done (PV completion, for rescaling and the epilogue).
+//  * Lazy rescale.  O and the denominator are rescaled only when a row's maximum grows by more
+//    than 2^8; the final O / l uses the same stale maximum, so the result is unchanged.  The
+//    decision is per row but TMEM loads/stores are warp-collective, so a warp rescales when
+//    any of its rows must (factor 1 for the others).
+//  * Epilogue.  O / l rounded to the input dtype, staged in the Q tile, TMA-stored per block.
+//  * Two CTAs share an SM, so one CTA's softmax also overlaps the other's MMAs.
+// Every mbarrier wait is bounded; on a timeout the CTA records TSA_ERR_TIMEOUT, drains its
+// in-flight copies and MMAs (bounded), frees TMEM and returns.
 #include <climits>
 
 #include "tsa_device.cuh"
@@ -28,33 +35,45 @@
 namespace tsa {
 namespace {
 
-constexpr int kRows = 128;           // query rows per CTA (two 64-token query blocks)
-constexpr int kBlock = 64;           // tokens per key / query block
-constexpr float kRescaleLog2 = 8.0f; // lazy-rescale threshold (log2 units)
+constexpr int kRows = 128;            // query rows per CTA (two 64-token query blocks)
+constexpr int kBlock = 64;            // tokens per key / query block
+constexpr int kStages = 2;            // K/V ring depth
+constexpr int kThreads = 192;         // 4 softmax warps + producer warp + MMA warp
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 
 template <int D>
 struct AttnSmem {
-    static constexpr int kChunks = D / 64;                  // 64-element (128 B) column chunks
-    static constexpr int kQBytes = kRows * D * 2;           // Q tile, later the O staging tile
-    static constexpr int kKVBytes = kBlock * D * 2;         // one K or V tile
-    static constexpr int kPBytes = kRows * kBlock * 2;      // P tile
+    static constexpr int kChunks = D / 64;            // 64-element (128 B) column chunks
+    static constexpr int kQBytes = kRows * D * 2;     // Q tile, later the O staging tile
+    static constexpr int kKVBytes = kBlock * D * 2;   // one K or V tile
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;           // 2 stages
-    static constexpr int kOffV = kOffK + 2 * kKVBytes;      // 2 stages
-    static constexpr int kOffP = kOffV + 2 * kKVBytes;
-    static constexpr int kOffMeta = kOffP + kPBytes;
-    static constexpr int kMetaBytes = 128;
-    static constexpr int kTmemCols = D == 128 ? 256 : 128;  // S (64 cols) + O (D cols)
-    static constexpr int kSCol = 0;
-    static constexpr int kOCol = 64;
+    static constexpr int kOffK = kOffQ + kQBytes;                // kStages tiles
+    static constexpr int kOffV = kOffK + kStages * kKVBytes;     // kStages tiles
+    static constexpr int kOffMeta = kOffV + kStages * kKVBytes;
+    static constexpr int kMetaBytes = 256;
+    static constexpr int kTmemCols = 256;  // S0 | S1 | O (P_b aliases the first 32 of S_b)
+    static constexpr int kOCol = 128;
 };
 
-// Meta area (byte offsets from kOffMeta).
-constexpr int kBarQ = 0, kBarKV = 8 /* 2 x 8 */, kBarMma = 24, kBarFin = 32;
-constexpr int kTmemSlot = 40, kMetaJ = 48 /* 2 x 4 */, kMetaF = 56 /* 2 x 4 */;
+__device__ __forceinline__ uint32_t s_col(int b) { return b ? 64u : 0u; }
+
+// Meta area layout (byte offsets from kOffMeta).
+constexpr int kBarQ = 0;
+constexpr int kBarKVFull = 8;    // kStages x 8
+constexpr int kBarKVEmpty = 24;  // kStages x 8
+constexpr int kBarSFull = 40;    // 2 x 8
+constexpr int kBarPFull = 56;    // 2 x 8
+constexpr int kBarODone = 72;
+constexpr int kBarFin = 80;
+constexpr int kTmemSlot = 88;
+constexpr int kAbortFlag = 92;
+constexpr int kMetaJ = 96;       // kStages x 4
+constexpr int kMetaF = 112;      // kStages x 4
 
 // Walks the union of two sorted CSR rows (query blocks qa and qa+1), checking the row
-// contract on the way.  Used by one thread.
+// contract on the way.  Used by the producer thread.
 struct RowUnion {
     const int32_t *col;
     int ia, ia_end, ib, ib_end;
@@ -99,8 +118,23 @@ struct RowUnion {
     }
 };
 
+// Two floats rounded to the 16-bit input dtype, packed (first in the low half); `sum` gets
+// the rounded values.
+template <bool kBF16>
+__device__ __forceinline__ uint32_t pack2(float a, float b, float &sum) {
+    if constexpr (kBF16) {
+        const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        sum += __low2float(h) + __high2float(h);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    } else {
+        const __half2 h = __floats2half2_rn(a, b);
+        sum += __low2float(h) + __high2float(h);
+        return *reinterpret_cast<const uint32_t *>(&h);
+    }
+}
+
 template <int D, bool kBF16>
-__global__ void __launch_bounds__(kRows, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV,
@@ -126,11 +160,15 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t sQ = base + L::kOffQ;
     const uint32_t sK0 = base + L::kOffK;
     const uint32_t sV0 = base + L::kOffV;
-    const uint32_t sP = base + L::kOffP;
     const uint32_t meta = base + L::kOffMeta;
-    const uint32_t bar_q = meta + kBarQ, bar_mma = meta + kBarMma, bar_fin = meta + kBarFin;
     volatile int *meta_j = reinterpret_cast<volatile int *>(smem + L::kOffMeta + kMetaJ);
     volatile int *meta_f = reinterpret_cast<volatile int *>(smem + L::kOffMeta + kMetaF);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMeta + kAbortFlag);
+    const uint32_t bar_q = meta + kBarQ, bar_o_done = meta + kBarODone, bar_fin = meta + kBarFin;
+#define BAR_KV_FULL(s) (meta + kBarKVFull + 8u * (uint32_t)(s))
+#define BAR_KV_EMPTY(s) (meta + kBarKVEmpty + 8u * (uint32_t)(s))
+#define BAR_S_FULL(b) (meta + kBarSFull + 8u * (uint32_t)(b))
+#define BAR_P_FULL(b) (meta + kBarPFull + 8u * (uint32_t)(b))
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -139,26 +177,25 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     const int pair = npairs - 1 - (int)blockIdx.x;   // longest rows first
     const int qa = 2 * pair;
     const bool has_b = qa + 1 < nb;
-    const int half = tid >> 6;                       // 0: block qa, 1: block qa+1
-    const int r_in = tid & 63;                       // token within the query block
-    const int my_block = qa + half;
-    const bool row_exists = half == 0 || has_b;
     const int row0 = lane_id * S;                    // first row of this lane in [L*S, D]
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        mbar_init(meta + kBarKV, 1);
-        mbar_init(meta + kBarKV + 8, 1);
-        mbar_init(bar_mma, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(BAR_KV_FULL(s), 1);
+            mbar_init(BAR_KV_EMPTY(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(BAR_S_FULL(b), 1);
+            mbar_init(BAR_P_FULL(b), kRows);
+        }
+        mbar_init(bar_o_done, 1);
         mbar_init(bar_fin, 1);
+        *abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
-        tma_prefetch_desc(&tmQ);
-        tma_prefetch_desc(&tmK);
-        tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmO);
     }
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tmem_alloc(meta + kTmemSlot, L::kTmemCols);
         tmem_relinquish();
     }
@@ -166,223 +203,249 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kOffMeta + kTmemSlot);
-    const uint32_t t_lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
 
-    // ---- producer state (thread 0): CSR row union and TMA issue
-    RowUnion ru;
-    int produced = 0;
-    auto produce = [&](int v) {
-        const int s = v & 1;
-        int f = 0;
-        const int j = ru.next(f);
-        meta_j[s] = j;
-        meta_f[s] = f;
-        const uint32_t bar = meta + kBarKV + 8 * s;
-        if (j < 0) {
-            mbar_arrive(bar);
-        } else {
-            mbar_arrive_expect_tx(bar, 2 * L::kKVBytes);
-            const int y = row0 + j * kBlock;
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------------ producer (TMA)
+        if ((tid & 31) == 0) {
+            tma_prefetch_desc(&tmQ);
+            tma_prefetch_desc(&tmK);
+            tma_prefetch_desc(&tmV);
+            tma_prefetch_desc(&tmO);
+            RowUnion ru;
+            ru.init(row_ptr, col_idx, qa, has_b);
+            mbar_arrive_expect_tx(bar_q, L::kQBytes);
 #pragma unroll
-            for (int c = 0; c < L::kChunks; ++c) {
-                tma_load_2d(sK0 + s * L::kKVBytes + c * 8192, &tmK, c * 64, y, bar);
-                tma_load_2d(sV0 + s * L::kKVBytes + c * 8192, &tmV, c * 64, y, bar);
+            for (int c = 0; c < L::kChunks; ++c)
+                tma_load_2d(sQ + c * 16384, &tmQ, c * 64, row0 + qa * kBlock, bar_q);
+            bool ok = true;
+            int v = 0;
+            for (;; ++v) {
+                const int s = v % kStages;
+                if (v >= kStages && !mbar_wait(BAR_KV_EMPTY(s), ((v / kStages) - 1) & 1, flags)) {
+                    ok = false;
+                    break;
+                }
+                int f = 0;
+                const int j = ru.next(f);
+                meta_j[s] = j;
+                meta_f[s] = f;
+                if (j < 0) {
+                    mbar_arrive(BAR_KV_FULL(s));
+                    break;
+                }
+                mbar_arrive_expect_tx(BAR_KV_FULL(s), 2 * L::kKVBytes);
+                const int y = row0 + j * kBlock;
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_load_2d(sK0 + s * L::kKVBytes + c * 8192, &tmK, c * 64, y, BAR_KV_FULL(s));
+                    tma_load_2d(sV0 + s * L::kKVBytes + c * 8192, &tmV, c * 64, y, BAR_KV_FULL(s));
+                }
+            }
+            if (ru.bad) raise_status(flags, kDevBadSchedule);
+            if (!ok) {
+                // Drain: wait (bounded) for every load issued into the ring.
+                *abort_flag = 1;
+                (void)mbar_wait_timed(bar_q, 0);
+                for (int w = v - kStages; w < v; ++w)
+                    if (w >= 0) (void)mbar_wait_timed(BAR_KV_FULL(w % kStages), (w / kStages) & 1);
             }
         }
-        produced = v + 1;
-    };
-    if (tid == 0) {
-        ru.init(row_ptr, col_idx, qa, has_b);
-        mbar_arrive_expect_tx(bar_q, L::kQBytes);
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if ((tid & 31) == 0) {
+            constexpr uint32_t kIdescQK = idesc_f16(kBF16, 128, 64, false);
+            constexpr uint32_t kIdescPV = idesc_f16(kBF16, 128, D, true);
+            bool ok = mbar_wait(bar_q, 0, flags);
+            int u = 0;
+            bool have = false;  // entry u exists and QK(u) was issued
+            if (ok) {
+                ok = mbar_wait(BAR_KV_FULL(0), 0, flags);
+                if (ok && meta_j[0] >= 0) have = true;
+            }
+            // QK(u): S_{u%2} = Q K_u^T
+#define ISSUE_QK(uu)                                                                              \
+    do {                                                                                          \
+        const int s_ = (uu) % kStages;                                                            \
+        tc_fence_after();                                                                         \
+        _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                   \
+            const uint64_t a_ = sdesc_sw128(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);    \
+            const uint64_t b_ =                                                                   \
+                sdesc_sw128(sK0 + s_ * L::kKVBytes + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024); \
+            tc_mma_ss(tmem + s_col((uu) & 1), a_, b_, kIdescQK, kk > 0 ? 1u : 0u);               \
+        }                                                                                         \
+        tc_commit(BAR_S_FULL((uu) & 1));                                                          \
+    } while (0)
+            if (have) ISSUE_QK(0);
+            while (ok && have) {
+                // next scores first, so they overlap the softmax of u
+                bool next = false;
+                const int s1 = (u + 1) % kStages;
+                ok = mbar_wait(BAR_KV_FULL(s1), ((u + 1) / kStages) & 1, flags);
+                if (!ok) break;
+                if (meta_j[s1] >= 0) {
+                    ISSUE_QK(u + 1);
+                    next = true;
+                }
+                // O += P_u V_u once the softmax has written P_u
+                ok = mbar_wait(BAR_P_FULL(u & 1), (u >> 1) & 1, flags);
+                if (!ok) break;
+                tc_fence_after();
+                const int s = u % kStages;
 #pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) tma_load_2d(sQ + c * 16384, &tmQ, c * 64, row0 + qa * kBlock, bar_q);
-        produce(0);
-        produce(1);
-    }
-
-    constexpr uint32_t kIdescQK = idesc_f16(kBF16, 128, 64, false);
-    constexpr uint32_t kIdescPV = idesc_f16(kBF16, 128, D, true);
-
-    float m_used = -INFINITY;  // maximum the accumulators are scaled to (log2 units)
-    float l_sum = 0.f;         // running denominator
-    bool o_valid = false;
-    bool aborted = false;
-    uint32_t mma_phase = 0;
-    bool ok = mbar_wait(bar_q, 0, flags);
-    int u = 0;
-    for (;; ++u) {
-        const int s = u & 1;
-        ok = mbar_wait(meta + kBarKV + 8 * s, (u >> 1) & 1, flags) && ok;
-        if (__syncthreads_or(!ok)) { aborted = true; break; }
-        const int j = meta_j[s];
-        const int fl = meta_f[s];
-        if (j < 0) break;
-
-        // S = Q K_j^T  (M 128, N 64, K D)
-        if (tid == 0) {
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t b = sdesc_sw128(sV0 + s * L::kKVBytes + kk * 2048, 8192, 1024);
+                    tc_mma_ts(tmem + L::kOCol, tmem + s_col(u & 1) + kk * 8, b, kIdescPV,
+                              (u > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(BAR_KV_EMPTY(s));
+                tc_commit(bar_o_done);
+                have = next;
+                ++u;
+            }
+#undef ISSUE_QK
+            if (!ok) *abort_flag = 1;
+            // all tensor-core work of this CTA has completed once this arrives
+            tc_commit(bar_fin);
+            (void)mbar_wait_timed(bar_fin, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (warps 0-3)
+        const int half = tid >> 6;               // 0: block qa, 1: block qa+1
+        const int r_in = tid & 63;               // token within the query block
+        const int my_block = qa + half;
+        const bool row_exists = half == 0 || has_b;
+        const uint32_t t_lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
+        float m_used = -INFINITY;                // maximum the accumulators are scaled to (log2)
+        float l_sum = 0.f;                       // running denominator
+        bool ok = true;
+        int u = 0;
+        for (;; ++u) {
+            const int s = u % kStages;
+            if (!mbar_wait(BAR_KV_FULL(s), (u / kStages) & 1, flags)) { ok = false; break; }
+            const int j = meta_j[s];
+            const int fl = meta_f[s];
+            if (j < 0) break;
+            if (!mbar_wait(BAR_S_FULL(u & 1), (u >> 1) & 1, flags)) { ok = false; break; }
             tc_fence_after();
+            const bool in_row = row_exists && ((fl >> half) & 1);  // warp-uniform
+            const uint32_t s_addr = tmem + t_lane + s_col(u & 1);
+            uint32_t pw[32];
+            __syncwarp();
+            if (in_row) {
+                uint32_t sr[2][32];
+                tmem_ld32(s_addr, sr[0]);
+                tmem_ld32(s_addr + 32, sr[1]);
+                const bool diag = (j == my_block);
+                float x[64];
+                float mx = -INFINITY;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint64_t a = sdesc_sw128(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                const uint64_t b = sdesc_sw128(sK0 + s * L::kKVBytes + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                tc_mma_ss(tmem + L::kSCol, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(bar_mma);
-        }
-        ok = mbar_wait(bar_mma, mma_phase, flags) && ok;
-        mma_phase ^= 1u;
-        tc_fence_after();
-
-        // ---- online softmax on this thread's row
-        const bool in_row = row_exists && ((fl >> half) & 1);  // warp-uniform
-        const uint32_t p_row = sP + tid * 128;
-        const uint32_t sw = (uint32_t)(tid & 7);
-        if (in_row) {
-            uint32_t sr[2][32];
-            __syncwarp();  // the waits above may leave the warp diverged; tcgen05.ld is collective
-            tmem_ld32(tmem + t_lane + L::kSCol, sr[0]);
-            tmem_ld32(tmem + t_lane + L::kSCol + 32, sr[1]);
-            const bool diag = (j == my_block);
-            float x[64];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                float v = __uint_as_float(sr[c >> 5][c & 31]) * scale_log2;
-                if (diag && c > r_in) v = -INFINITY;
-                x[c] = v;
-                mx = fmaxf(mx, v);
-            }
-            // The rescale decision is per row, but tcgen05.ld/st are warp-collective: the whole
-            // warp rescales when any of its rows must, with factor 1 for the other rows.
-            const bool grow = mx > m_used + kRescaleLog2;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : ex2_approx(m_used - mx));
-                if (o_valid) {
-                    __syncwarp();
-#pragma unroll
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(tmem + t_lane + L::kOCol + c, o);
-#pragma unroll
-                        for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
-                        tmem_st32(tmem + t_lane + L::kOCol + c, o);
-                    }
+                for (int c = 0; c < 64; ++c) {
+                    float v = __uint_as_float(sr[c >> 5][c & 31]) * scale_log2;
+                    if (diag && c > r_in) v = -INFINITY;
+                    x[c] = v;
+                    mx = fmaxf(mx, v);
                 }
-                if (grow) {
-                    l_sum *= alpha;
-                    m_used = mx;
-                }
-            }
-            float lsum_blk = 0.f;
+                const bool grow = mx > m_used + kRescaleLog2;
+                if (__any_sync(0xffffffffu, grow)) {
+                    const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : ex2_approx(m_used - mx));
+                    if (u > 0) {
+                        // O must be quiescent: PV(u-1) has completed
+                        const bool done = mbar_wait(bar_o_done, (u - 1) & 1, flags);
+                        if (__any_sync(0xffffffffu, !done)) { ok = false; break; }
+                        tc_fence_after();
+                        __syncwarp();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                uint32_t w[4];
+                        for (int c = 0; c < D; c += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(tmem + t_lane + L::kOCol + c, o);
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float p0 = ex2_approx(x[q * 8 + 2 * t] - m_used);
-                    const float p1 = ex2_approx(x[q * 8 + 2 * t + 1] - m_used);
-                    if constexpr (kBF16) {
-                        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-                        lsum_blk += __low2float(h) + __high2float(h);
-                        w[t] = *reinterpret_cast<const uint32_t *>(&h);
-                    } else {
-                        const __half2 h = __floats2half2_rn(p0, p1);
-                        lsum_blk += __low2float(h) + __high2float(h);
-                        w[t] = *reinterpret_cast<const uint32_t *>(&h);
-                    }
-                }
-                st_shared_v4(p_row + (((uint32_t)q ^ sw) << 4), w[0], w[1], w[2], w[3]);
-            }
-            l_sum += lsum_blk;
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) st_shared_v4(p_row + (q << 4), 0u, 0u, 0u, 0u);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (__syncthreads_or(!ok)) { aborted = true; break; }
-
-        // O += P V_j  (M 128, N D, K 64); V is MN-major (d contiguous)
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t a = sdesc_sw128(sP + kk * 32, 16, 1024);
-                const uint64_t b = sdesc_sw128(sV0 + s * L::kKVBytes + kk * 2048, 8192, 1024);
-                tc_mma_ss(tmem + L::kOCol, a, b, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc_commit(bar_mma);
-        }
-        ok = mbar_wait(bar_mma, mma_phase, flags) && ok;
-        mma_phase ^= 1u;
-        tc_fence_after();
-        o_valid = true;
-        if (tid == 0) produce(u + 2);
-    }
-
-    if (tid == 0 && ru.bad) raise_status(flags, kDevBadSchedule);
-
-    if (!aborted) {
-        // ---- epilogue: O / l in the input dtype, staged in the Q tile, TMA store per block
-        const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-        const uint32_t sw = (uint32_t)(tid & 7);
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < L::kChunks; ++c) {
-            const uint32_t o_row = sQ + c * 16384 + tid * 128;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t o[32];
-                if (o_valid) {
-                    tmem_ld32(tmem + t_lane + L::kOCol + c * 64 + h * 32, o);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) o[t] = 0u;
-                }
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const float a = __uint_as_float(o[q * 8 + 2 * t]) * inv;
-                        const float b = __uint_as_float(o[q * 8 + 2 * t + 1]) * inv;
-                        if constexpr (kBF16) {
-                            const __nv_bfloat162 hv = __floats2bfloat162_rn(a, b);
-                            w[t] = *reinterpret_cast<const uint32_t *>(&hv);
-                        } else {
-                            const __half2 hv = __floats2half2_rn(a, b);
-                            w[t] = *reinterpret_cast<const uint32_t *>(&hv);
+                            for (int t = 0; t < 32; ++t) o[t] = __float_as_uint(__uint_as_float(o[t]) * alpha);
+                            tmem_st32(tmem + t_lane + L::kOCol + c, o);
                         }
                     }
-                    const uint32_t chunk16 = (uint32_t)(h * 4 + q);
-                    st_shared_v4(o_row + ((chunk16 ^ sw) << 4), w[0], w[1], w[2], w[3]);
+                    if (grow) {
+                        l_sum *= alpha;
+                        m_used = mx;
+                    }
                 }
+                float lsum_blk = 0.f;
+#pragma unroll
+                for (int t = 0; t < 32; ++t)
+                    pw[t] = pack2<kBF16>(ex2_approx(x[2 * t] - m_used), ex2_approx(x[2 * t + 1] - m_used),
+                                         lsum_blk);
+                l_sum += lsum_blk;
+            } else {
+#pragma unroll
+                for (int t = 0; t < 32; ++t) pw[t] = 0u;
             }
+            __syncwarp();
+            tmem_st32(s_addr, pw);  // P_u over the first 32 columns of S_u
+            tc_fence_before();
+            mbar_arrive(BAR_P_FULL(u & 1));
         }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        if (!ok) *abort_flag = 1;
+        // ---- epilogue: O / l in the input dtype, staged in the Q tile, TMA-stored per block
+        bool o_valid = false;
+        if (ok && u > 0) {
+            o_valid = mbar_wait(bar_o_done, (u - 1) & 1, flags);
+            if (!o_valid) *abort_flag = 1;
+        }
+        named_barrier(1, kRows);
+        if (*abort_flag == 0) {
+            tc_fence_after();
+            const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            const uint32_t sw = (uint32_t)(tid & 7);
+            __syncwarp();
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
-                tma_store_2d(&tmO, c * 64, row0 + qa * kBlock, sQ + c * 16384);
-                if (has_b) tma_store_2d(&tmO, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
+                const uint32_t o_row = sQ + c * 16384 + tid * 128;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t o[32];
+                    if (o_valid) {
+                        tmem_ld32(tmem + t_lane + L::kOCol + c * 64 + h * 32, o);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) o[t] = 0u;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float unused = 0.f;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            w[t] = pack2<kBF16>(__uint_as_float(o[q * 8 + 2 * t]) * inv,
+                                                __uint_as_float(o[q * 8 + 2 * t + 1]) * inv, unused);
+                        const uint32_t chunk16 = (uint32_t)(h * 4 + q);
+                        st_shared_v4(o_row + ((chunk16 ^ sw) << 4), w[0], w[1], w[2], w[3]);
+                    }
+                }
             }
-            tma_store_commit();
-            tma_store_wait_all();
+            fence_proxy_async_smem();
+            named_barrier(1, kRows);
+            if (tid == 0) {
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c) {
+                    tma_store_2d(&tmO, c * 64, row0 + qa * kBlock, sQ + c * 16384);
+                    if (has_b) tma_store_2d(&tmO, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
+                }
+                tma_store_commit();
+                tma_store_wait_all();
+            }
         }
-    } else if (tid == 0) {
-        // Gave up: record it, then let in-flight tensor-core work and TMA loads drain (bounded)
-        // before the shared memory and TMEM are released.
-        raise_status(flags, kDevTimeout);
-        atomicExch(flags.abort_epoch, flags.epoch);
-        tc_commit(bar_fin);
-        (void)mbar_wait_timed(bar_fin, 0);
-        (void)mbar_wait_timed(bar_q, 0);
-        for (int v = u; v < produced; ++v) (void)mbar_wait_timed(meta + kBarKV + 8 * (v & 1), (v >> 1) & 1);
     }
+#undef BAR_KV_FULL
+#undef BAR_KV_EMPTY
+#undef BAR_S_FULL
+#undef BAR_P_FULL
+
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (threadIdx.x == 0 && *abort_flag) {
+        raise_status(flags, kDevTimeout);
+        atomicExch(flags.abort_epoch, flags.epoch);
+    }
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, L::kTmemCols);
     }
@@ -396,9 +459,8 @@ tsa_status launch_one(const AttnLaunch &a) {
         return TSA_ERR_CUDA;
     const int npairs = (a.nb + 1) / 2;
     dim3 grid((unsigned)npairs, (unsigned)a.lanes);
-    kern<<<grid, kRows, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
-                                                         a.col_idx, a.nb, a.S, a.scale_log2,
-                                                         a.flags);
+    kern<<<grid, kThreads, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
+                                                            a.col_idx, a.nb, a.S, a.scale_log2, a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }
 

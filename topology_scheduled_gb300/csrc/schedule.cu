@@ -20,7 +20,8 @@
 //   pairwise_d2        nb x nb squared distances, tiles with u-tile <= v-tile (FP64 ALU)
 //   boruvka_*          ceil(log2 nb) rounds: per-vertex lightest edge (all CTAs), then one
 //                      CTA picks per-component edges, hooks and relabels
-//   elder_salience     one CTA: bitonic sort of the nb-1 MST edges, sequential union-find
+//   elder_salience     one CTA: bitonic sort of the nb-1 MST edges; one warp then merges in
+//                      edge order, every block carrying its root label
 //   topk_csr           one CTA: salience order, per-row bitmaps, row counts, scan, fill
 #include <climits>
 
@@ -38,10 +39,75 @@ __device__ __forceinline__ double widen(uint16_t bits, bool bf16) {
 }
 
 // ---------------------------------------------------------------- centroids
-// part[l][b][d] = sum_{t=0}^{block-1} K[l][b*block+t][d], t ascending; 8 d per thread.
+// part[l][b][d] = sum_{t=0}^{block-1} K[l][b*block+t][d], added in ascending t in binary64.
+//
+// FP64 runs at a small fraction of the FP32 rate on this part, so the sum is formed exactly
+// in int64 fixed point whenever that provably equals the sequential binary64 sum:
+//  * f16 elements are integer multiples of 2^-24 below 2^16 in magnitude, so every partial
+//    sum of up to 4096 of them is a multiple of 2^-24 below 2^40 * 2^12 = 2^52: exactly
+//    representable, hence the sequential binary64 sum is exact and equals the integer sum.
+//  * bf16 elements with biased exponent e hold (128 + frac) * 2^(e - 134).  If all non-zero
+//    elements of a column have e in [94, 142] (ulp >= 2^-40, |x| < 2^16), the column fits an
+//    int64 in units of 2^-40 (block <= 64: |sum| < 2^62).  If moreover e_max - e_min <=
+//    45 - ceil(log2(block)), every partial sum is a multiple of 2^(e_min - 134) below
+//    2^(e_max - 126) * block <= 2^(e_min - 134 + 53), so again the sequential binary64 sum is
+//    exact and equals the integer sum.
+// A column that meets neither condition (subnormal, huge or widely spread values, inf/nan)
+// is summed again the plain way, in binary64 in ascending t.
+struct ColumnSum {
+    long long acc;
+    int emin, emax;
+    bool bad;
+};
+
+__device__ __forceinline__ void col_init(ColumnSum &c) {
+    c.acc = 0;
+    c.emin = 1 << 20;
+    c.emax = -(1 << 20);
+    c.bad = false;
+}
+
+__device__ __forceinline__ void col_add(ColumnSum &c, uint32_t h, bool bf16) {
+    const bool neg = (h & 0x8000u) != 0;
+    long long mag;
+    if (bf16) {
+        const int e = (int)((h >> 7) & 0xFFu);
+        const bool nonzero = (h & 0x7FFFu) != 0;
+        const bool in_window = e >= 94 && e <= 142;
+        const int sh = in_window ? e - 94 : 0;
+        mag = (long long)((h & 0x7Fu) | 0x80u) << sh;
+        if (!nonzero) mag = 0;
+        if (nonzero) {
+            c.emin = min(c.emin, e);
+            c.emax = max(c.emax, e);
+            c.bad |= !in_window;
+        }
+    } else {
+        const int e = (int)((h >> 10) & 0x1Fu);
+        const uint32_t f = h & 0x3FFu;
+        c.bad |= (e == 31);
+        mag = e ? ((long long)(0x400u | f) << (e - 1)) : (long long)f;  // units of 2^-24, < 2^40
+    }
+    c.acc += neg ? -mag : mag;
+}
+
+// True when the integer sum equals the sequential binary64 sum (see above).
+__device__ __forceinline__ bool col_exact(const ColumnSum &c, bool bf16, int64_t block,
+                                          int spread_limit) {
+    if (c.bad) return false;
+    if (!bf16) return block <= 4096;
+    if (block > 64) return false;
+    return c.emax < c.emin || c.emax - c.emin <= spread_limit;  // emax < emin: all zero
+}
+
+__device__ __forceinline__ double col_value(const ColumnSum &c, bool bf16) {
+    return bf16 ? ldexp((double)c.acc, -40) : ldexp((double)c.acc, -24);
+}
+
+// One thread per (lane, block, 8 consecutive d); 16-byte loads.
 __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
                                       int64_t S, int64_t D, int64_t block, int64_t nb,
-                                      double *__restrict__ part) {
+                                      int spread_limit, double *__restrict__ part) {
     const int64_t groups = D / 8;
     const int64_t total = lanes * nb * groups;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
@@ -50,9 +116,9 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
         const int64_t lb = w / groups;  // l * nb + b
         const int64_t l = lb / nb, b = lb % nb;
         const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
-        double acc[8];
+        ColumnSum c[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = 0.0;
+        for (int i = 0; i < 8; ++i) col_init(c[i]);
         int64_t t = 0;
         for (; t + 8 <= block; t += 8) {
             uint4 v[8];
@@ -63,8 +129,8 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
                 const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] += widen((uint16_t)(w4[i] & 0xFFFFu), bf16);
-                    acc[2 * i + 1] += widen((uint16_t)(w4[i] >> 16), bf16);
+                    col_add(c[2 * i], w4[i] & 0xFFFFu, bf16);
+                    col_add(c[2 * i + 1], w4[i] >> 16, bf16);
                 }
             }
         }
@@ -73,20 +139,28 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                acc[2 * i] += widen((uint16_t)(w4[i] & 0xFFFFu), bf16);
-                acc[2 * i + 1] += widen((uint16_t)(w4[i] >> 16), bf16);
+                col_add(c[2 * i], w4[i] & 0xFFFFu, bf16);
+                col_add(c[2 * i + 1], w4[i] >> 16, bf16);
             }
         }
         double *dst = part + lb * D + g * 8;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = acc[i];
+        for (int i = 0; i < 8; ++i) {
+            if (col_exact(c[i], bf16, block, spread_limit)) {
+                dst[i] = col_value(c[i], bf16);
+            } else {
+                double acc = 0.0;
+                for (int64_t tt = 0; tt < block; ++tt) acc += widen(__ldg(src + tt * D + i), bf16);
+                dst[i] = acc;
+            }
+        }
     }
 }
 
 // Same sums, one d per thread (any D, any alignment).
 __global__ void centroid_partial_scalar(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
                                         int64_t S, int64_t D, int64_t block, int64_t nb,
-                                        double *__restrict__ part) {
+                                        int spread_limit, double *__restrict__ part) {
     const int64_t total = lanes * nb * D;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
          w += (int64_t)gridDim.x * blockDim.x) {
@@ -94,9 +168,16 @@ __global__ void centroid_partial_scalar(const uint16_t *__restrict__ K, bool bf1
         const int64_t lb = w / D;
         const int64_t l = lb / nb, b = lb % nb;
         const uint16_t *src = K + (l * S + b * block) * D + d;
-        double acc = 0.0;
-        for (int64_t t = 0; t < block; ++t) acc += widen(__ldg(src + t * D), bf16);
-        part[w] = acc;
+        ColumnSum c;
+        col_init(c);
+        for (int64_t t = 0; t < block; ++t) col_add(c, __ldg(src + t * D), bf16);
+        if (col_exact(c, bf16, block, spread_limit)) {
+            part[w] = col_value(c, bf16);
+        } else {
+            double acc = 0.0;
+            for (int64_t t = 0; t < block; ++t) acc += widen(__ldg(src + t * D), bf16);
+            part[w] = acc;
+        }
     }
 }
 
@@ -113,22 +194,25 @@ __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, i
 }
 
 // ---------------------------------------------------------------- pairwise distances
-constexpr int kPdTile = 32;   // pairs per tile side
+constexpr int kPdTile = 16;   // pairs per tile side
 constexpr int kPdChunk = 32;  // d values staged per step
 
-// D2[u][v] = D2[v][u] = sum_{d ascending} fma((C[u][d]-C[v][d]), same, acc); only tiles with
-// u-tile <= v-tile run; each thread computes a 2 x 2 block of pairs.
-__global__ void __launch_bounds__(256) pairwise_d2(const double *__restrict__ C, int64_t nb,
-                                                   int64_t D, double *__restrict__ D2) {
-    const int tu = blockIdx.y, tv = blockIdx.x;
-    if (tu > tv) return;
+// D2[u][v] = D2[v][u] = sum_{d ascending} fma(C[u][d]-C[v][d], same, acc).  One CTA per tile
+// (tu <= tv) of the upper triangle, 64 threads, 2 x 2 pairs each.  (C[v]-C[u] is exactly
+// -(C[u]-C[v]), so the mirrored entry is bit-identical to computing it directly.)
+__global__ void __launch_bounds__(64) pairwise_d2(const double *__restrict__ C, int64_t nb,
+                                                  int64_t D, int tiles, double *__restrict__ D2) {
     __shared__ double cu[kPdTile][kPdChunk + 1];
     __shared__ double cv[kPdTile][kPdChunk + 1];
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    // linear tile index -> (tu, tv), tu <= tv, row-major over the upper triangle
+    int k = blockIdx.x, tu = 0;
+    while (k >= tiles - tu) { k -= tiles - tu; ++tu; }
+    const int tv = tu + k;
+    const int tx = threadIdx.x & 7, ty = threadIdx.x >> 3;
     const int64_t u0 = (int64_t)tu * kPdTile, v0 = (int64_t)tv * kPdTile;
     double acc[2][2] = {{0.0, 0.0}, {0.0, 0.0}};
     for (int64_t d0 = 0; d0 < D; d0 += kPdChunk) {
-        for (int i = threadIdx.x; i < kPdTile * kPdChunk; i += 256) {
+        for (int i = threadIdx.x; i < kPdTile * kPdChunk; i += 64) {
             const int r = i / kPdChunk, c = i % kPdChunk;
             const int64_t d = d0 + c;
             cu[r][c] = (u0 + r < nb && d < D) ? C[(u0 + r) * D + d] : 0.0;
@@ -136,25 +220,26 @@ __global__ void __launch_bounds__(256) pairwise_d2(const double *__restrict__ C,
         }
         __syncthreads();
         const int dn = (int)((D - d0) < kPdChunk ? (D - d0) : kPdChunk);
+#pragma unroll 4
         for (int c = 0; c < dn; ++c) {
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const double delta = cu[ty * 2 + i][c] - cv[tx * 2 + k][c];
-                    acc[i][k] = fma(delta, delta, acc[i][k]);
-                }
+            const double a0 = cu[ty * 2][c], a1 = cu[ty * 2 + 1][c];
+            const double b0 = cv[tx * 2][c], b1 = cv[tx * 2 + 1][c];
+            double t;
+            t = a0 - b0; acc[0][0] = fma(t, t, acc[0][0]);
+            t = a0 - b1; acc[0][1] = fma(t, t, acc[0][1]);
+            t = a1 - b0; acc[1][0] = fma(t, t, acc[1][0]);
+            t = a1 - b1; acc[1][1] = fma(t, t, acc[1][1]);
         }
         __syncthreads();
     }
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int64_t u = u0 + ty * 2 + i, v = v0 + tx * 2 + k;
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const int64_t u = u0 + ty * 2 + i, v = v0 + tx * 2 + k2;
             if (u < nb && v < nb) {
-                D2[u * nb + v] = acc[i][k];
-                D2[v * nb + u] = acc[i][k];
+                D2[u * nb + v] = acc[i][k2];
+                D2[v * nb + u] = acc[i][k2];
             }
         }
 }
@@ -307,20 +392,14 @@ __device__ void bitonic_sort_pairs(unsigned long long *k1, unsigned long long *k
     }
 }
 
-// Root of x with path halving (which never changes a root); -1 if more than `limit` hops,
-// which a forest never needs.
-__device__ __forceinline__ int dsu_find(volatile int *parent, int x, int limit) {
-    for (int hops = 0; parent[x] != x; ++hops) {
-        if (hops > limit) return -1;
-        const int g = parent[parent[x]];
-        parent[x] = g;
-        x = g;
-    }
-    return x;
-}
-
 // Kruskal order over the MST edges; the smaller component is absorbed (size tie: the root
 // with the larger index); the absorbed root receives the edge's d2; one block keeps 0.
+// After the sort, one warp runs the merges.  Every block carries its component's root label;
+// lane l keeps the labels of blocks l, l+32, ... in registers (kLabelRegs of them, so up to
+// 32 * kLabelRegs blocks) and mirrors them in shared memory, where the two roots of an edge
+// are read.  A merge relabels the absorbed component with a register scan.
+constexpr int kLabelRegs = 32;
+
 __global__ void __launch_bounds__(1024) elder_salience(int nb, const int *__restrict__ counters,
                                                        const double *__restrict__ mst_d,
                                                        const int *__restrict__ mst_u,
@@ -330,8 +409,8 @@ __global__ void __launch_bounds__(1024) elder_salience(int nb, const int *__rest
     extern __shared__ __align__(16) uint8_t sm[];
     unsigned long long *kd = reinterpret_cast<unsigned long long *>(sm);
     unsigned long long *kab = kd + pow2;
-    volatile int *parent = reinterpret_cast<volatile int *>(kab + pow2);
-    volatile int *size = parent + nb;
+    volatile int *label = reinterpret_cast<volatile int *>(kab + pow2);
+    volatile int *size = label + nb;
     const int ne = nb - 1;
     if (threadIdx.x == 0 && counters[1] != ne) raise_status(flags, kDevCapacity);
     for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
@@ -344,28 +423,50 @@ __global__ void __launch_bounds__(1024) elder_salience(int nb, const int *__rest
         }
     }
     for (int v = threadIdx.x; v < nb; v += blockDim.x) {
-        parent[v] = v;
+        label[v] = v;
         size[v] = 1;
         sal[v] = 0.0;
     }
     __syncthreads();
     bitonic_sort_pairs(kd, kab, pow2);
-    if (threadIdx.x == 0) {
-        for (int e = 0; e < ne; ++e) {
-            const int a = (int)(kab[e] >> 32), b = (int)(kab[e] & 0xFFFFFFFFu);
-            if (a < 0 || a >= nb || b < 0 || b >= nb) { raise_status(flags, kDevCapacity); break; }
-            const int ra = dsu_find(parent, a, nb), rb = dsu_find(parent, b, nb);
-            if (ra < 0 || rb < 0) { raise_status(flags, kDevCapacity); break; }
-            if (ra == rb) continue;
-            const int sa = size[ra], sb = size[rb];
-            int absorbed, survivor;
-            if (sa < sb) { absorbed = ra; survivor = rb; }
-            else if (sb < sa) { absorbed = rb; survivor = ra; }
-            else { absorbed = ra > rb ? ra : rb; survivor = ra > rb ? rb : ra; }
-            sal[absorbed] = __longlong_as_double((long long)kd[e]);
-            parent[absorbed] = survivor;
-            size[survivor] = sa + sb;
+    if (threadIdx.x >= 32) return;
+    const int lane = threadIdx.x;
+    const bool in_regs = nb <= 32 * kLabelRegs;
+    int lab[kLabelRegs];
+#pragma unroll
+    for (int k = 0; k < kLabelRegs; ++k) lab[k] = lane + 32 * k;
+    for (int e = 0; e < ne; ++e) {
+        const unsigned long long ab = kab[e];
+        const int a = (int)(ab >> 32), b = (int)(ab & 0xFFFFFFFFu);
+        if (a < 0 || a >= nb || b < 0 || b >= nb) {
+            if (lane == 0) raise_status(flags, kDevCapacity);
+            break;
         }
+        const int ra = label[a], rb = label[b];
+        if (ra == rb) continue;  // cannot happen for MST edges
+        const int sa = size[ra], sb = size[rb];
+        int absorbed, survivor;
+        if (sa < sb) { absorbed = ra; survivor = rb; }
+        else if (sb < sa) { absorbed = rb; survivor = ra; }
+        else { absorbed = ra > rb ? ra : rb; survivor = ra > rb ? rb : ra; }
+        __syncwarp();
+        if (in_regs) {
+#pragma unroll
+            for (int k = 0; k < kLabelRegs; ++k) {
+                if (lab[k] == absorbed) {
+                    lab[k] = survivor;
+                    label[lane + 32 * k] = survivor;
+                }
+            }
+        } else {
+            for (int v = lane; v < nb; v += 32)
+                if (label[v] == absorbed) label[v] = survivor;
+        }
+        if (lane == 0) {
+            size[survivor] = sa + sb;
+            sal[absorbed] = __longlong_as_double((long long)kd[e]);
+        }
+        __syncwarp();
     }
 }
 
@@ -593,10 +694,15 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
     const int threads = 256;
     const int64_t blocks = (items + threads - 1) / threads;
     const unsigned grid = (unsigned)(blocks < 152 * 64 ? blocks : 152 * 64);
+    int log2_block = 0;
+    while ((int64_t(1) << log2_block) < a.block) ++log2_block;
+    const int spread_limit = 45 - log2_block;
     if (vec)
-        centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb, part);
+        centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
+                                                        spread_limit, part);
     else
-        centroid_partial_scalar<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb, part);
+        centroid_partial_scalar<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
+                                                          spread_limit, part);
     {
         const int64_t n = a.nb * a.D;
         const unsigned g = (unsigned)((n + 255) / 256);
@@ -604,8 +710,8 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
     }
     // distances
     {
-        const unsigned t = (unsigned)((nb + kPdTile - 1) / kPdTile);
-        pairwise_d2<<<dim3(t, t), 256, 0, st>>>(cent, a.nb, a.D, d2);
+        const int t = (nb + kPdTile - 1) / kPdTile;
+        pairwise_d2<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(cent, a.nb, a.D, t, d2);
     }
     // Boruvka MST
     boruvka_init<<<(nb + 255) / 256, 256, 0, st>>>(comp, nb, counters);

@@ -177,6 +177,23 @@ __device__ __forceinline__ void tc_mma_ss(uint32_t d_tmem, uint64_t adesc, uint6
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc]: A (M x K, 16-bit) read from tensor memory, row m in
+// lane m, elements k = 2c and 2c+1 packed in 32-bit column c.
+__device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) with id `id` (1..15).
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Instruction descriptor for kind::f16 with fp32 accumulation.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16, 1 = bf16),
 //   bit 15 A major (0 = K-major), bit 16 B major (1 = MN-major), 17-22 N >> 3, 24-28 M >> 4.
