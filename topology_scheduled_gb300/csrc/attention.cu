@@ -335,16 +335,23 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 uint32_t sr[2][32];
                 tmem_ld32(s_addr, sr[0]);
                 tmem_ld32(s_addr + 32, sr[1]);
-                const bool diag = (j == my_block);
-                float x[64];
-                float mx = -INFINITY;
+                float x[64];  // raw scores q.k
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    float v = __uint_as_float(sr[c >> 5][c & 31]) * scale_log2;
-                    if (diag && c > r_in) v = -INFINITY;
-                    x[c] = v;
-                    mx = fmaxf(mx, v);
+                for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
+                if (j == my_block) {  // diagonal block: keys after the query token are masked
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c > r_in) x[c] = -INFINITY;
                 }
+                float m21[22];
+#pragma unroll
+                for (int t = 0; t < 21; ++t) m21[t] = max3f(x[3 * t], x[3 * t + 1], x[3 * t + 2]);
+                m21[21] = x[63];
+                const float m7a = max3f(max3f(m21[0], m21[1], m21[2]), max3f(m21[3], m21[4], m21[5]),
+                                        max3f(m21[6], m21[7], m21[8]));
+                const float m7b = max3f(max3f(m21[9], m21[10], m21[11]), max3f(m21[12], m21[13], m21[14]),
+                                        max3f(m21[15], m21[16], m21[17]));
+                const float mx = max3f(m7a, m7b, max3f(m21[18], m21[19], fmaxf(m21[20], m21[21]))) * scale_log2;
                 const bool grow = mx > m_used + kRescaleLog2;
                 if (__any_sync(0xffffffffu, grow)) {
                     const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : ex2_approx(m_used - mx));
@@ -368,12 +375,34 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         m_used = mx;
                     }
                 }
-                float lsum_blk = 0.f;
+                // p = 2^(x * scale * log2(e) - m): one packed FMA per pair, exp2 on the MUFU
+                const uint64_t cc = f2_pack(scale_log2, scale_log2);
+                const uint64_t nm = f2_pack(-m_used, -m_used);
+                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    pw[t] = pack2<kBF16>(ex2_approx(x[2 * t] - m_used), ex2_approx(x[2 * t + 1] - m_used),
-                                         lsum_blk);
-                l_sum += lsum_blk;
+                for (int t = 0; t < 32; ++t) {
+                    float e0, e1;
+                    f2_unpack(f2_fma(f2_pack(x[2 * t], x[2 * t + 1]), cc, nm), e0, e1);
+                    const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
+                    // The denominator sums the rounded P that the PV product uses, so a row
+                    // dominated by one key normalizes exactly.
+                    uint64_t rounded;
+                    if constexpr (kBF16) {
+                        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+                        pw[t] = *reinterpret_cast<const uint32_t *>(&h);
+                        rounded = f2_pack(__uint_as_float(pw[t] << 16), __uint_as_float(pw[t] & 0xFFFF0000u));
+                    } else {
+                        const __half2 h = __floats2half2_rn(p0, p1);
+                        pw[t] = *reinterpret_cast<const uint32_t *>(&h);
+                        rounded = f2_pack(__low2float(h), __high2float(h));
+                    }
+                    if (t & 1) acc1 = f2_add(acc1, rounded);
+                    else acc0 = f2_add(acc0, rounded);
+                }
+                float a0, a1, b0, b1;
+                f2_unpack(acc0, a0, a1);
+                f2_unpack(acc1, b0, b1);
+                l_sum += (a0 + b0) + (a1 + b1);
             } else {
 #pragma unroll
                 for (int t = 0; t < 32; ++t) pw[t] = 0u;
