@@ -16,9 +16,12 @@
 //    softmax, one row per thread: tcgen05.ld of the S row, exp2 with the scale folded in, the
 //    new P written back over the S buffer in the input dtype with tcgen05.st.
 //  * Pipeline.  The MMA warp issues QK(u+1) before PV(u), so the tensor core computes the next
-//    scores while the softmax warps work on the current ones.  Hand-offs are mbarriers:
-//    kv_full/kv_empty (producer <-> MMA), s_full (MMA -> softmax), p_full (softmax -> MMA),
-//    o_done (PV completion, for rescaling and the epilogue).
+//    scores while the softmax warps work on the current ones.  K and V have rings of their
+//    own: a K stage is refilled as soon as its QK is done, so the next key tile is already
+//    resident when the MMA warp reaches it.  Hand-offs are mbarriers: k_full/k_empty and
+//    v_full/v_empty (producer <-> MMA), s_full (MMA -> softmax, also carries the end of the
+//    row union), p_full (softmax -> MMA), o_done (PV completion, for rescaling and the
+//    epilogue).
 //  * Lazy rescale.  O and the denominator are rescaled only when a row's maximum grows by more
 //    than 2^8; the final O / l uses the same stale maximum, so the result is unchanged.  The
 //    decision is per row but TMEM loads/stores are warp-collective, so a warp rescales when
@@ -60,17 +63,20 @@ struct AttnSmem {
 __device__ __forceinline__ uint32_t s_col(int b) { return b ? 64u : 0u; }
 
 // Meta area layout (byte offsets from kOffMeta).
+constexpr int kMetaRing = 4;     // union entries in flight (K ring runs up to 2 ahead of softmax)
 constexpr int kBarQ = 0;
-constexpr int kBarKVFull = 8;    // kStages x 8
-constexpr int kBarKVEmpty = 24;  // kStages x 8
-constexpr int kBarSFull = 40;    // 2 x 8
-constexpr int kBarPFull = 56;    // 2 x 8
-constexpr int kBarODone = 72;
-constexpr int kBarFin = 80;
-constexpr int kTmemSlot = 88;
-constexpr int kAbortFlag = 92;
-constexpr int kMetaJ = 96;       // kStages x 4
-constexpr int kMetaF = 112;      // kStages x 4
+constexpr int kBarKFull = 8;     // kStages x 8
+constexpr int kBarKEmpty = 24;   // kStages x 8
+constexpr int kBarVFull = 40;    // kStages x 8
+constexpr int kBarVEmpty = 56;   // kStages x 8
+constexpr int kBarSFull = 72;    // 2 x 8
+constexpr int kBarPFull = 88;    // 2 x 8
+constexpr int kBarODone = 104;
+constexpr int kBarFin = 112;
+constexpr int kTmemSlot = 120;
+constexpr int kAbortFlag = 124;
+constexpr int kMetaJ = 128;      // kMetaRing x 4
+constexpr int kMetaF = 144;      // kMetaRing x 4
 
 // Walks the union of two sorted CSR rows (query blocks qa and qa+1), checking the row
 // contract on the way.  Used by the producer thread.
@@ -165,8 +171,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     volatile int *meta_f = reinterpret_cast<volatile int *>(smem + L::kOffMeta + kMetaF);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMeta + kAbortFlag);
     const uint32_t bar_q = meta + kBarQ, bar_o_done = meta + kBarODone, bar_fin = meta + kBarFin;
-#define BAR_KV_FULL(s) (meta + kBarKVFull + 8u * (uint32_t)(s))
-#define BAR_KV_EMPTY(s) (meta + kBarKVEmpty + 8u * (uint32_t)(s))
+#define BAR_K_FULL(s) (meta + kBarKFull + 8u * (uint32_t)(s))
+#define BAR_K_EMPTY(s) (meta + kBarKEmpty + 8u * (uint32_t)(s))
+#define BAR_V_FULL(s) (meta + kBarVFull + 8u * (uint32_t)(s))
+#define BAR_V_EMPTY(s) (meta + kBarVEmpty + 8u * (uint32_t)(s))
 #define BAR_S_FULL(b) (meta + kBarSFull + 8u * (uint32_t)(b))
 #define BAR_P_FULL(b) (meta + kBarPFull + 8u * (uint32_t)(b))
 
@@ -182,8 +190,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (tid == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(BAR_KV_FULL(s), 1);
-            mbar_init(BAR_KV_EMPTY(s), 1);
+            mbar_init(BAR_K_FULL(s), 1);
+            mbar_init(BAR_K_EMPTY(s), 1);
+            mbar_init(BAR_V_FULL(s), 1);
+            mbar_init(BAR_V_EMPTY(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(BAR_S_FULL(b), 1);
@@ -217,37 +227,44 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
                 tma_load_2d(sQ + c * 16384, &tmQ, c * 64, row0 + qa * kBlock, bar_q);
+            // Entry v: K into stage v % kStages once QK(v - kStages) is done, V into its stage
+            // once PV(v - kStages) is done; K therefore runs ahead of V.
             bool ok = true;
-            int v = 0;
+            int v = 0, k_issued = 0, v_issued = 0;
             for (;; ++v) {
                 const int s = v % kStages;
-                if (v >= kStages && !mbar_wait(BAR_KV_EMPTY(s), ((v / kStages) - 1) & 1, flags)) {
-                    ok = false;
-                    break;
-                }
+                const uint32_t par = (uint32_t)((v / kStages) - 1) & 1u;
+                if (v >= kStages && !mbar_wait(BAR_K_EMPTY(s), par, flags)) { ok = false; break; }
                 int f = 0;
                 const int j = ru.next(f);
-                meta_j[s] = j;
-                meta_f[s] = f;
+                meta_j[v % kMetaRing] = j;
+                meta_f[v % kMetaRing] = f;
                 if (j < 0) {
-                    mbar_arrive(BAR_KV_FULL(s));
+                    mbar_arrive(BAR_K_FULL(s));
                     break;
                 }
-                mbar_arrive_expect_tx(BAR_KV_FULL(s), 2 * L::kKVBytes);
                 const int y = row0 + j * kBlock;
+                mbar_arrive_expect_tx(BAR_K_FULL(s), L::kKVBytes);
 #pragma unroll
-                for (int c = 0; c < L::kChunks; ++c) {
-                    tma_load_2d(sK0 + s * L::kKVBytes + c * 8192, &tmK, c * 64, y, BAR_KV_FULL(s));
-                    tma_load_2d(sV0 + s * L::kKVBytes + c * 8192, &tmV, c * 64, y, BAR_KV_FULL(s));
-                }
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_2d(sK0 + s * L::kKVBytes + c * 8192, &tmK, c * 64, y, BAR_K_FULL(s));
+                k_issued = v + 1;
+                if (v >= kStages && !mbar_wait(BAR_V_EMPTY(s), par, flags)) { ok = false; break; }
+                mbar_arrive_expect_tx(BAR_V_FULL(s), L::kKVBytes);
+#pragma unroll
+                for (int c = 0; c < L::kChunks; ++c)
+                    tma_load_2d(sV0 + s * L::kKVBytes + c * 8192, &tmV, c * 64, y, BAR_V_FULL(s));
+                v_issued = v + 1;
             }
             if (ru.bad) raise_status(flags, kDevBadSchedule);
             if (!ok) {
-                // Drain: wait (bounded) for every load issued into the ring.
+                // Drain: wait (bounded) for every load issued into the rings.
                 *abort_flag = 1;
                 (void)mbar_wait_timed(bar_q, 0);
-                for (int w = v - kStages; w < v; ++w)
-                    if (w >= 0) (void)mbar_wait_timed(BAR_KV_FULL(w % kStages), (w / kStages) & 1);
+                for (int w = k_issued - kStages; w < k_issued; ++w)
+                    if (w >= 0) (void)mbar_wait_timed(BAR_K_FULL(w % kStages), (w / kStages) & 1);
+                for (int w = v_issued - kStages; w < v_issued; ++w)
+                    if (w >= 0) (void)mbar_wait_timed(BAR_V_FULL(w % kStages), (w / kStages) & 1);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -258,11 +275,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             bool ok = mbar_wait(bar_q, 0, flags);
             int u = 0;
             bool have = false;  // entry u exists and QK(u) was issued
-            if (ok) {
-                ok = mbar_wait(BAR_KV_FULL(0), 0, flags);
-                if (ok && meta_j[0] >= 0) have = true;
-            }
-            // QK(u): S_{u%2} = Q K_u^T
+            // QK(u): S_{u%2} = Q K_u^T; frees K stage u % kStages when done
 #define ISSUE_QK(uu)                                                                              \
     do {                                                                                          \
         const int s_ = (uu) % kStages;                                                            \
@@ -274,30 +287,47 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             tc_mma_ss(tmem + s_col((uu) & 1), a_, b_, kIdescQK, kk > 0 ? 1u : 0u);               \
         }                                                                                         \
         tc_commit(BAR_S_FULL((uu) & 1));                                                          \
+        tc_commit(BAR_K_EMPTY(s_));                                                               \
     } while (0)
-            if (have) ISSUE_QK(0);
+            // The end of the row union is passed to the softmax warps as an s_full arrival
+            // without scores (they read the end marker from the meta ring).
+            if (ok) {
+                ok = mbar_wait(BAR_K_FULL(0), 0, flags);
+                if (ok) {
+                    if (meta_j[0] >= 0) {
+                        ISSUE_QK(0);
+                        have = true;
+                    } else {
+                        mbar_arrive(BAR_S_FULL(0));
+                    }
+                }
+            }
             while (ok && have) {
                 // next scores first, so they overlap the softmax of u
                 bool next = false;
                 const int s1 = (u + 1) % kStages;
-                ok = mbar_wait(BAR_KV_FULL(s1), ((u + 1) / kStages) & 1, flags);
+                ok = mbar_wait(BAR_K_FULL(s1), ((u + 1) / kStages) & 1, flags);
                 if (!ok) break;
-                if (meta_j[s1] >= 0) {
+                if (meta_j[(u + 1) % kMetaRing] >= 0) {
                     ISSUE_QK(u + 1);
                     next = true;
+                } else {
+                    mbar_arrive(BAR_S_FULL((u + 1) & 1));
                 }
-                // O += P_u V_u once the softmax has written P_u
+                // O += P_u V_u once the softmax has written P_u and V_u has landed
                 ok = mbar_wait(BAR_P_FULL(u & 1), (u >> 1) & 1, flags);
                 if (!ok) break;
-                tc_fence_after();
                 const int s = u % kStages;
+                ok = mbar_wait(BAR_V_FULL(s), (u / kStages) & 1, flags);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const uint64_t b = sdesc_sw128(sV0 + s * L::kKVBytes + kk * 2048, 8192, 1024);
                     tc_mma_ts(tmem + L::kOCol, tmem + s_col(u & 1) + kk * 8, b, kIdescPV,
                               (u > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc_commit(BAR_KV_EMPTY(s));
+                tc_commit(BAR_V_EMPTY(s));
                 tc_commit(bar_o_done);
                 have = next;
                 ++u;
@@ -320,12 +350,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         bool ok = true;
         int u = 0;
         for (;; ++u) {
-            const int s = u % kStages;
-            if (!mbar_wait(BAR_KV_FULL(s), (u / kStages) & 1, flags)) { ok = false; break; }
-            const int j = meta_j[s];
-            const int fl = meta_f[s];
-            if (j < 0) break;
             if (!mbar_wait(BAR_S_FULL(u & 1), (u >> 1) & 1, flags)) { ok = false; break; }
+            const int j = meta_j[u % kMetaRing];
+            const int fl = meta_f[u % kMetaRing];
+            if (j < 0) break;
             tc_fence_after();
             const bool in_row = row_exists && ((fl >> half) & 1);  // warp-uniform
             const uint32_t s_addr = tmem + t_lane + s_col(u & 1);
@@ -463,8 +491,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             }
         }
     }
-#undef BAR_KV_FULL
-#undef BAR_KV_EMPTY
+#undef BAR_K_FULL
+#undef BAR_K_EMPTY
+#undef BAR_V_FULL
+#undef BAR_V_EMPTY
 #undef BAR_S_FULL
 #undef BAR_P_FULL
 
