@@ -15,14 +15,11 @@
 //              selects the same tree as Kruskal in the oracle.
 //
 // Kernels, in stream order:
-//   centroid_partial   per (lane, block, d): sum of the block's tokens     (HBM stream of K)
-//   centroid_final     per (block, d): sum over lanes, divide               (small)
-//   pairwise_d2        nb x nb squared distances, tiles with u-tile <= v-tile (FP64 ALU)
-//   boruvka_*          ceil(log2 nb) rounds: per-vertex lightest edge (all CTAs), then one
-//                      CTA picks per-component edges, hooks and relabels
-//   elder_salience     one CTA: bitonic sort of the nb-1 MST edges; one warp then merges in
-//                      edge order, every block carrying its root label
-//   topk_csr           one CTA: salience order, per-row bitmaps, row counts, scan, fill
+//   centroid_partial      per (lane, block, d): sum of the block's tokens   (HBM stream of K)
+//   centroid_final        per (block, d): sum over lanes, divide             (small)
+//   pairwise_d2           nb x nb squared distances over the upper triangle  (FP64 ALU)
+//   schedule_graph_kernel one cooperative launch: Boruvka MST, elder-rule salience, top-k
+//                         CSR (see the section comment below)
 #include <climits>
 
 #include "tsa_device.cuh"
@@ -104,18 +101,105 @@ __device__ __forceinline__ double col_value(const ColumnSum &c, bool bf16) {
     return bf16 ? ldexp((double)c.acc, -40) : ldexp((double)c.acc, -24);
 }
 
+// Sequential binary64 sum of one column (the reference order), used for columns that none
+// of the exact fast paths covers.
+__device__ double column_sum_exact_slow(const uint16_t *src, int64_t D, int64_t block, bool bf16,
+                                        int spread_limit) {
+    ColumnSum c;
+    col_init(c);
+    for (int64_t t = 0; t < block; ++t) col_add(c, __ldg(src + t * D), bf16);
+    if (col_exact(c, bf16, block, spread_limit)) return col_value(c, bf16);
+    double acc = 0.0;
+    for (int64_t t = 0; t < block; ++t) acc += widen(__ldg(src + t * D), bf16);
+    return acc;
+}
+
 // One thread per (lane, block, 8 consecutive d); 16-byte loads.
+//
+// bf16 fast path: the column is summed as an unevaluated pair hi + lo of fp32 values (packed
+// two columns at a time).  Each step is Knuth's TwoSum, which splits hi + x exactly into the
+// rounded sum and its error; the errors collect in lo.  Every element and every error is an
+// integer multiple of 2^(e_min - 134), each error is below 2^(e_max - 143) in magnitude, so
+// lo's partial sums (64 of them) need at most e_max - e_min - 4 significant bits: with
+// e_max - e_min <= 28 (biased exponents of the non-zero elements, from the packed 16-bit
+// max/min of |bits|; subnormals count as exponent 1; no inf/nan) lo is exact, hence
+// hi + lo is the exact column sum.  That sum has at most e_max - e_min + 14 <= 42 significant
+// bits, so the sequential binary64 sum is exact too and both equal (double)hi + (double)lo.
+// Other columns (and f16, and blocks longer than 64) take the int64 path above.
 __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
                                       int64_t S, int64_t D, int64_t block, int64_t nb,
                                       int spread_limit, double *__restrict__ part) {
     const int64_t groups = D / 8;
     const int64_t total = lanes * nb * groups;
+    const bool fp32_path = bf16 && block <= 64;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
          w += (int64_t)gridDim.x * blockDim.x) {
         const int64_t g = w % groups;
         const int64_t lb = w / groups;  // l * nb + b
         const int64_t l = lb / nb, b = lb % nb;
         const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
+        double *dst = part + lb * D + g * 8;
+        if (fp32_path) {
+            uint64_t hi[4], lo[4];
+            uint32_t mx[4], mn[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                hi[i] = f2_pack(0.f, 0.f);
+                lo[i] = hi[i];
+                mx[i] = 0u;
+                mn[i] = 0xFFFFFFFFu;
+            }
+            // hi + lo += x exactly (TwoSum), two columns per packed operation
+            auto two_sum = [&](int i, uint32_t x) {
+                const uint64_t v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+                const uint64_t s = f2_add(hi[i], v);
+                const uint64_t bv = f2_sub(s, hi[i]);
+                const uint64_t err = f2_add(f2_sub(hi[i], f2_sub(s, bv)), f2_sub(v, bv));
+                lo[i] = f2_add(lo[i], err);
+                hi[i] = s;
+                const uint32_t a = x & 0x7FFF7FFFu;
+                mx[i] = __vmaxu2(mx[i], a);
+                mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
+            };
+            int64_t t = 0;
+            for (; t + 8 <= block; t += 8) {
+                uint4 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + (t + u) * D));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    two_sum(0, v[u].x);
+                    two_sum(1, v[u].y);
+                    two_sum(2, v[u].z);
+                    two_sum(3, v[u].w);
+                }
+            }
+            for (; t < block; ++t) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
+                two_sum(0, v.x);
+                two_sum(1, v.y);
+                two_sum(2, v.z);
+                two_sum(3, v.w);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float h0, h1, l0, l1;
+                f2_unpack(hi[i], h0, h1);
+                f2_unpack(lo[i], l0, l1);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
+                    const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
+                    const int emax = (int)(amax >> 7);
+                    const int emin = max(1, (int)(amin >> 7));
+                    const bool all_zero = amin == 0xFFFFu;
+                    const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
+                    dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
+                                           : column_sum_exact_slow(src + 2 * i + h, D, block, bf16, spread_limit);
+                }
+            }
+            continue;
+        }
         ColumnSum c[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) col_init(c[i]);
@@ -143,7 +227,6 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
                 col_add(c[2 * i + 1], w4[i] >> 16, bf16);
             }
         }
-        double *dst = part + lb * D + g * 8;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (col_exact(c[i], bf16, block, spread_limit)) {
@@ -244,11 +327,72 @@ __global__ void __launch_bounds__(64) pairwise_d2(const double *__restrict__ C, 
         }
 }
 
-// ---------------------------------------------------------------- Boruvka MST
-struct EdgeKey {
-    double d;
-    int a, b;  // a < b
+// ---------------------------------------------------------------- MST, elder rule, CSR
+// One cooperative launch runs everything after the distance matrix.  Its CTAs are all
+// resident (cudaLaunchCooperativeKernel), so they can meet at grid-wide barriers; the barrier
+// is bounded in time like every other wait here.
+//   Boruvka rounds: all warps find each vertex's lightest edge to another component (strict
+//     key (d2, min(u,v), max(u,v))); CTA 0 takes each component's lightest edge, hooks along
+//     it (a mutual pair keeps the smaller label as root), records each chosen edge once,
+//     flattens by pointer jumping and relabels.  The rounds stop at one component.
+//   Elder rule (CTA 0): bitonic sort of the nb-1 MST edges by the same key, then one warp
+//     merges in that order: the smaller component is absorbed (size tie: the root with the
+//     larger index) and its root receives the edge's d2.
+//   CSR: every CTA sorts the blocks by (salience desc, index asc); warps count each row's
+//     blocks from a per-row bitmap (sink range, local window, first topk blocks <= i of the
+//     order); CTA 0 scans the counts into row_ptr; warps fill col_idx in ascending order.
+struct GraphArgs {
+    const double *d2;
+    int nb, pow2, sink, r, topk, rounds;
+    size_t xs_offset;  // byte offset of the sort exchange buffer in dynamic shared memory
+    int *comp;
+    double *vb_d;
+    int *vb_u;
+    double *mst_d;
+    int *mst_u, *mst_v;
+    int *counters;   // [0] components, [1] MST edges recorded, [2] CSR overflow
+    unsigned *gbar;  // [0] arrivals, [1] generation, [2] gave up
+    double *sal;
+    int *cnt;        // per-row counts, then row starts
+    int32_t *row_ptr, *col_idx;
+    int64_t col_cap;
+    DeviceFlags flags;
 };
+
+// Grid-wide barrier (generation counter).  Returns false for the whole grid once any CTA has
+// given up waiting.
+__device__ bool grid_sync(unsigned *gbar, const DeviceFlags &f) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        volatile unsigned *vg = gbar;
+        int ok = vg[2] == 0u;
+        if (ok) {
+            const unsigned gen = vg[1];
+            __threadfence();
+            if (atomicAdd(&gbar[0], 1u) == gridDim.x - 1) {
+                atomicExch(&gbar[0], 0u);
+                __threadfence();
+                atomicAdd(&gbar[1], 1u);
+            } else {
+                const unsigned long long t0 = globaltimer();
+                while (vg[1] == gen) {
+                    if (vg[2] != 0u) { ok = 0; break; }
+                    if (globaltimer() - t0 > kWaitTimeoutNs) {
+                        atomicExch(&gbar[2], 1u);
+                        raise_status(f, kDevTimeout);
+                        ok = 0;
+                        break;
+                    }
+                }
+            }
+            __threadfence();
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
 
 __device__ __forceinline__ bool key_less(double d1, int a1, int b1, double d2, int a2, int b2) {
     if (d1 < d2) return true;
@@ -257,94 +401,95 @@ __device__ __forceinline__ bool key_less(double d1, int a1, int b1, double d2, i
     return b1 < b2;
 }
 
-__global__ void boruvka_init(int *__restrict__ comp, int nb, int *__restrict__ counters) {
-    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < nb; v += gridDim.x * blockDim.x) comp[v] = v;
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        counters[0] = nb;  // components
-        counters[1] = 0;   // MST edges recorded
-    }
-}
-
-// One warp per vertex v: the lightest edge from v to another component.
-__global__ void boruvka_vertex_min(const double *__restrict__ D2, const int *__restrict__ comp,
-                                   int nb, const int *__restrict__ counters,
-                                   double *__restrict__ vb_d, int *__restrict__ vb_u) {
-    if (counters[0] <= 1) return;
+// Each vertex's lightest edge to another component; one warp per vertex, grid-wide.  Every
+// CTA keeps its own copy of the component labels in shared memory (`scomp`); each lane reads
+// its d2 entries in independent batches of 8.
+__device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, double *vb_d, int *vb_u) {
+    const int nb = a.nb;
     const int lane = threadIdx.x & 31;
-    const int v = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (v >= nb) return;
-    const int cv = comp[v];
-    double bd = __longlong_as_double((long long)kInfBits);
-    int ba = INT_MAX, bb = INT_MAX, bu = -1;
-    const double *row = D2 + (int64_t)v * nb;
-    for (int u = lane; u < nb; u += 32) {
-        if (comp[u] == cv) continue;
-        const double d = row[u];
-        const int a = u < v ? u : v, b = u < v ? v : u;
-        if (key_less(d, a, b, bd, ba, bb)) { bd = d; ba = a; bb = b; bu = u; }
-    }
+    const int wpb = blockDim.x >> 5;
+    const int total = gridDim.x * wpb;
+    for (int v = blockIdx.x * wpb + (threadIdx.x >> 5); v < nb; v += total) {
+        const int cv = scomp[v];
+        double bd = __longlong_as_double((long long)kInfBits);
+        int ba = INT_MAX, bb = INT_MAX, bu = -1;
+        const double *row = a.d2 + (int64_t)v * nb;
+        for (int u0 = lane; u0 < nb; u0 += 32 * 8) {
+            double d[8];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const double od = __shfl_xor_sync(0xffffffffu, bd, off);
-        const int oa = __shfl_xor_sync(0xffffffffu, ba, off);
-        const int ob = __shfl_xor_sync(0xffffffffu, bb, off);
-        const int ou = __shfl_xor_sync(0xffffffffu, bu, off);
-        if (key_less(od, oa, ob, bd, ba, bb)) { bd = od; ba = oa; bb = ob; bu = ou; }
-    }
-    if (lane == 0) {
-        vb_d[v] = bd;
-        vb_u[v] = bu;
+            for (int k = 0; k < 8; ++k) {
+                const int u = u0 + 32 * k;
+                d[k] = u < nb ? __ldg(row + u) : 0.0;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int u = u0 + 32 * k;
+                if (u < nb && scomp[u] != cv) {
+                    const int x = u < v ? u : v, y = u < v ? v : u;
+                    if (key_less(d[k], x, y, bd, ba, bb)) { bd = d[k]; ba = x; bb = y; bu = u; }
+                }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const double od = __shfl_xor_sync(0xffffffffu, bd, off);
+            const int oa = __shfl_xor_sync(0xffffffffu, ba, off);
+            const int ob = __shfl_xor_sync(0xffffffffu, bb, off);
+            const int ou = __shfl_xor_sync(0xffffffffu, bu, off);
+            if (key_less(od, oa, ob, bd, ba, bb)) { bd = od; ba = oa; bb = ob; bu = ou; }
+        }
+        if (lane == 0) {
+            vb_d[v] = bd;
+            vb_u[v] = bu;
+        }
     }
 }
 
-// One CTA: per component the lightest outgoing edge (min over its vertices), hook along it
-// (a mutual pair keeps the smaller label as root), record each chosen edge once, flatten by
-// pointer jumping and relabel.
-__global__ void __launch_bounds__(1024) boruvka_merge(int *__restrict__ comp, int nb,
-                                                      int *__restrict__ counters,
-                                                      const double *__restrict__ vb_d,
-                                                      const int *__restrict__ vb_u,
-                                                      double *__restrict__ mst_d,
-                                                      int *__restrict__ mst_u,
-                                                      int *__restrict__ mst_v) {
-    if (counters[0] <= 1) return;
-    extern __shared__ __align__(16) uint8_t sm[];
+// Every CTA, on its own shared-memory copy: per component the lightest outgoing edge (min
+// over its vertices), hooking (a mutual pair keeps the smaller label as root), flattening by
+// pointer jumping and relabelling.  All CTAs compute the same result; CTA 0 also records the
+// chosen edges.  Returns the number of components left.
+__device__ int merge_phase(const GraphArgs &a, uint8_t *sm, int *scomp, const double *vb_d,
+                           const int *vb_u, int *n_edges) {
+    const int nb = a.nb;
     unsigned long long *cb_d = reinterpret_cast<unsigned long long *>(sm);
     unsigned long long *cb_ab = cb_d + nb;
     volatile int *par = reinterpret_cast<volatile int *>(cb_ab + nb);
     __shared__ int s_roots, s_edges;
     const int tid = threadIdx.x, nt = blockDim.x;
-    if (tid == 0) { s_roots = 0; s_edges = counters[1]; }
+    const bool record = blockIdx.x == 0;
+    if (tid == 0) { s_roots = 0; s_edges = *n_edges; }
     for (int c = tid; c < nb; c += nt) {
         cb_d[c] = kInfBits;
         cb_ab[c] = ~0ull;
     }
     __syncthreads();
     for (int v = tid; v < nb; v += nt)
-        atomicMin(&cb_d[comp[v]], (unsigned long long)__double_as_longlong(vb_d[v]));
+        atomicMin(&cb_d[scomp[v]], (unsigned long long)__double_as_longlong(__ldcg(vb_d + v)));
     __syncthreads();
     for (int v = tid; v < nb; v += nt) {
-        const int c = comp[v];
-        if ((unsigned long long)__double_as_longlong(vb_d[v]) == cb_d[c] && vb_u[v] >= 0) {
-            const unsigned a = (unsigned)min(v, vb_u[v]), b = (unsigned)max(v, vb_u[v]);
-            atomicMin(&cb_ab[c], ((unsigned long long)a << 32) | b);
+        const int c = scomp[v];
+        const int u = __ldcg(vb_u + v);
+        if ((unsigned long long)__double_as_longlong(__ldcg(vb_d + v)) == cb_d[c] && u >= 0) {
+            const unsigned x = (unsigned)min(v, u), y = (unsigned)max(v, u);
+            atomicMin(&cb_ab[c], ((unsigned long long)x << 32) | y);
         }
     }
     __syncthreads();
     for (int c = tid; c < nb; c += nt) {
-        if (comp[c] != c) continue;
+        if (scomp[c] != c) continue;
         const unsigned long long ab = cb_ab[c];
         if (ab == ~0ull) { par[c] = c; continue; }
-        const int a = (int)(ab >> 32), b = (int)(ab & 0xFFFFFFFFu);
-        const int other = comp[a] == c ? comp[b] : comp[a];
+        const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
+        const int other = scomp[x] == c ? scomp[y] : scomp[x];
         const bool mutual = cb_ab[other] == ab;
         par[c] = (mutual && c < other) ? c : other;
-        if (!mutual || c < other) {
+        if (record && (!mutual || c < other)) {
             const int idx = atomicAdd(&s_edges, 1);
             if (idx < nb - 1) {
-                mst_d[idx] = __longlong_as_double((long long)cb_d[c]);
-                mst_u[idx] = a;
-                mst_v[idx] = b;
+                a.mst_d[idx] = __longlong_as_double((long long)cb_d[c]);
+                a.mst_u[idx] = x;
+                a.mst_v[idx] = y;
             }
         }
     }
@@ -352,7 +497,7 @@ __global__ void __launch_bounds__(1024) boruvka_merge(int *__restrict__ comp, in
     for (int iter = 0; iter < 64; ++iter) {
         int changed = 0;
         for (int c = tid; c < nb; c += nt) {
-            if (comp[c] != c) continue;
+            if (scomp[c] != c) continue;
             const int p = par[c];
             const int pp = par[p];
             if (p != pp) { par[c] = pp; changed = 1; }
@@ -360,17 +505,16 @@ __global__ void __launch_bounds__(1024) boruvka_merge(int *__restrict__ comp, in
         if (!__syncthreads_or(changed)) break;
     }
     for (int c = tid; c < nb; c += nt)
-        if (comp[c] == c && par[c] == c) atomicAdd(&s_roots, 1);
+        if (scomp[c] == c && par[c] == c) atomicAdd(&s_roots, 1);
     __syncthreads();
-    for (int v = tid; v < nb; v += nt) comp[v] = par[comp[v]];
+    for (int v = tid; v < nb; v += nt) scomp[v] = par[scomp[v]];
     __syncthreads();
-    if (tid == 0) {
-        counters[0] = s_roots;
-        counters[1] = s_edges;
-    }
+    const int roots = s_roots;
+    if (tid == 0) *n_edges = s_edges;
+    __syncthreads();
+    return roots;
 }
 
-// ---------------------------------------------------------------- elder rule
 // Sort 64-bit key pairs ascending (lexicographic on (k1, k2)); n is a power of two.
 __device__ void bitonic_sort_pairs(unsigned long long *k1, unsigned long long *k2, int n) {
     for (int size = 2; size <= n; size <<= 1) {
@@ -392,31 +536,68 @@ __device__ void bitonic_sort_pairs(unsigned long long *k1, unsigned long long *k
     }
 }
 
-// Kruskal order over the MST edges; the smaller component is absorbed (size tie: the root
-// with the larger index); the absorbed root receives the edge's d2; one block keeps 0.
-// After the sort, one warp runs the merges.  Every block carries its component's root label;
-// lane l keeps the labels of blocks l, l+32, ... in registers (kLabelRegs of them, so up to
-// 32 * kLabelRegs blocks) and mirrors them in shared memory, where the two roots of an edge
-// are read.  A merge relabels the absorbed component with a register scan.
-constexpr int kLabelRegs = 32;
+// Bitonic sort of (k1, k2) pairs ascending with one element per thread (n == blockDim.x, a
+// power of two): strides below 32 exchange through shuffles, larger ones through `xs`
+// (2 * n words of shared memory).  On return k1/k2 hold the element of rank threadIdx.x.
+__device__ void bitonic_sort_regs(unsigned long long &k1, unsigned long long &k2,
+                                  unsigned long long *xs) {
+    const int i = threadIdx.x, n = blockDim.x;
+    for (int size = 2; size <= n; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            unsigned long long p1, p2;
+            if (stride < 32) {
+                p1 = __shfl_xor_sync(0xffffffffu, k1, stride);
+                p2 = __shfl_xor_sync(0xffffffffu, k2, stride);
+            } else {
+                xs[i] = k1;
+                xs[n + i] = k2;
+                __syncthreads();
+                p1 = xs[i ^ stride];
+                p2 = xs[n + (i ^ stride)];
+                __syncthreads();
+            }
+            const bool ascending = (i & size) == 0;
+            const bool lower = (i & stride) == 0;
+            const bool mine_less = k1 < p1 || (k1 == p1 && k2 < p2);
+            const bool take_partner = (ascending == lower) ? !mine_less : mine_less;
+            if (take_partner) {
+                k1 = p1;
+                k2 = p2;
+            }
+        }
+    }
+}
 
-__global__ void __launch_bounds__(1024) elder_salience(int nb, const int *__restrict__ counters,
-                                                       const double *__restrict__ mst_d,
-                                                       const int *__restrict__ mst_u,
-                                                       const int *__restrict__ mst_v, int pow2,
-                                                       double *__restrict__ sal,
-                                                       DeviceFlags flags) {
-    extern __shared__ __align__(16) uint8_t sm[];
+// 16-way select of v[s] (s in [0, 16)) as a depth-4 tree of selects (no local memory).
+__device__ __forceinline__ int select16(const int (&v)[16], int s) {
+    int t[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = (s & 1) ? v[2 * k + 1] : v[2 * k];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) t[k] = (s & 2) ? t[2 * k + 1] : t[2 * k];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) t[k] = (s & 4) ? t[2 * k + 1] : t[2 * k];
+    return (s & 8) ? t[1] : t[0];
+}
+
+// Lane l of the merging warp keeps the root labels of blocks l, l+32, ... in registers (up
+// to 32 * kLabelRegs blocks; beyond that the labels live in shared memory).  A root label is
+// read with a branch-free select of the slot and a shuffle from the owning lane.
+constexpr int kLabelRegs = 16;
+
+// CTA 0: elder-rule salience from the MST edges.
+__device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsigned long long *xs) {
+    const int nb = a.nb, pow2 = a.pow2;
     unsigned long long *kd = reinterpret_cast<unsigned long long *>(sm);
     unsigned long long *kab = kd + pow2;
-    volatile int *label = reinterpret_cast<volatile int *>(kab + pow2);
-    volatile int *size = label + nb;
+    volatile int *size = reinterpret_cast<volatile int *>(kab + pow2);
+    volatile int *label = size + nb;  // used only when nb > 32 * kLabelRegs
     const int ne = nb - 1;
-    if (threadIdx.x == 0 && counters[1] != ne) raise_status(flags, kDevCapacity);
+    if (threadIdx.x == 0 && n_edges != ne) raise_status(a.flags, kDevCapacity);
     for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
         if (i < ne) {
-            kd[i] = (unsigned long long)__double_as_longlong(mst_d[i]);
-            kab[i] = ((unsigned long long)(unsigned)mst_u[i] << 32) | (unsigned)mst_v[i];
+            kd[i] = (unsigned long long)__double_as_longlong(a.mst_d[i]);
+            kab[i] = ((unsigned long long)(unsigned)a.mst_u[i] << 32) | (unsigned)a.mst_v[i];
         } else {
             kd[i] = ~0ull;
             kab[i] = ~0ull;
@@ -425,61 +606,94 @@ __global__ void __launch_bounds__(1024) elder_salience(int nb, const int *__rest
     for (int v = threadIdx.x; v < nb; v += blockDim.x) {
         label[v] = v;
         size[v] = 1;
-        sal[v] = 0.0;
+        a.sal[v] = 0.0;
     }
     __syncthreads();
-    bitonic_sort_pairs(kd, kab, pow2);
-    if (threadIdx.x >= 32) return;
-    const int lane = threadIdx.x;
-    const bool in_regs = nb <= 32 * kLabelRegs;
-    int lab[kLabelRegs];
-#pragma unroll
-    for (int k = 0; k < kLabelRegs; ++k) lab[k] = lane + 32 * k;
-    for (int e = 0; e < ne; ++e) {
-        const unsigned long long ab = kab[e];
-        const int a = (int)(ab >> 32), b = (int)(ab & 0xFFFFFFFFu);
-        if (a < 0 || a >= nb || b < 0 || b >= nb) {
-            if (lane == 0) raise_status(flags, kDevCapacity);
-            break;
+    const bool fast = nb <= 32 * kLabelRegs && pow2 <= (int)blockDim.x;
+    if (fast) {
+        // one element per thread (padding sorts last), sorted copy written back to kd/kab
+        unsigned long long k1 = threadIdx.x < pow2 ? kd[threadIdx.x] : ~0ull;
+        unsigned long long k2 = threadIdx.x < pow2 ? kab[threadIdx.x] : ~0ull;
+        __syncthreads();
+        bitonic_sort_regs(k1, k2, xs);
+        __syncthreads();
+        if (threadIdx.x < pow2) {
+            kd[threadIdx.x] = k1;
+            kab[threadIdx.x] = k2;
         }
-        const int ra = label[a], rb = label[b];
-        if (ra == rb) continue;  // cannot happen for MST edges
-        const int sa = size[ra], sb = size[rb];
-        int absorbed, survivor;
-        if (sa < sb) { absorbed = ra; survivor = rb; }
-        else if (sb < sa) { absorbed = rb; survivor = ra; }
-        else { absorbed = ra > rb ? ra : rb; survivor = ra > rb ? rb : ra; }
-        __syncwarp();
-        if (in_regs) {
+        __syncthreads();
+    } else {
+        bitonic_sort_pairs(kd, kab, pow2);
+    }
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        if (fast) {
+            // Everything in registers: lane l holds the root label and, for roots, the
+            // component size of blocks l + 32k; edges arrive 32 at a time and are broadcast.
+            int lab[kLabelRegs], sz[kLabelRegs];
 #pragma unroll
             for (int k = 0; k < kLabelRegs; ++k) {
-                if (lab[k] == absorbed) {
-                    lab[k] = survivor;
-                    label[lane + 32 * k] = survivor;
+                lab[k] = lane + 32 * k;
+                sz[k] = 1;
+            }
+            for (int e0 = 0; e0 < ne; e0 += 32) {
+                const unsigned long long my_ab = e0 + lane < ne ? kab[e0 + lane] : 0ull;
+                const unsigned long long my_d = e0 + lane < ne ? kd[e0 + lane] : 0ull;
+                const int cnt = min(32, ne - e0);
+                for (int j = 0; j < cnt; ++j) {
+                    const unsigned long long ab = __shfl_sync(0xffffffffu, my_ab, j);
+                    const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
+                    const int rx = __shfl_sync(0xffffffffu, select16(lab, (x >> 5) & 15), x & 31);
+                    const int ry = __shfl_sync(0xffffffffu, select16(lab, (y >> 5) & 15), y & 31);
+                    const int sx = __shfl_sync(0xffffffffu, select16(sz, (rx >> 5) & 15), rx & 31);
+                    const int sy = __shfl_sync(0xffffffffu, select16(sz, (ry >> 5) & 15), ry & 31);
+                    int absorbed, survivor;
+                    if (sx < sy) { absorbed = rx; survivor = ry; }
+                    else if (sy < sx) { absorbed = ry; survivor = rx; }
+                    else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
+                    const bool merge = rx != ry;  // always true for MST edges
+                    const bool owner = lane == (survivor & 31);
+#pragma unroll
+                    for (int k = 0; k < kLabelRegs; ++k) {
+                        lab[k] = (merge && lab[k] == absorbed) ? survivor : lab[k];
+                        sz[k] = (merge && owner && k == (survivor >> 5)) ? sx + sy : sz[k];
+                    }
+                    if (merge && lane == j)
+                        a.sal[absorbed] = __longlong_as_double((long long)my_d);
                 }
             }
         } else {
-            for (int v = lane; v < nb; v += 32)
-                if (label[v] == absorbed) label[v] = survivor;
+            for (int e = 0; e < ne; ++e) {
+                const unsigned long long ab = kab[e];
+                const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
+                if (x < 0 || x >= nb || y < 0 || y >= nb) {
+                    if (lane == 0) raise_status(a.flags, kDevCapacity);
+                    break;
+                }
+                const int rx = label[x], ry = label[y];
+                if (rx == ry) continue;  // cannot happen for MST edges
+                const int sx = size[rx], sy = size[ry];
+                int absorbed, survivor;
+                if (sx < sy) { absorbed = rx; survivor = ry; }
+                else if (sy < sx) { absorbed = ry; survivor = rx; }
+                else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
+                __syncwarp();
+                for (int v = lane; v < nb; v += 32)
+                    if (label[v] == absorbed) label[v] = survivor;
+                if (lane == 0) {
+                    size[survivor] = sx + sy;
+                    a.sal[absorbed] = __longlong_as_double((long long)kd[e]);
+                }
+                __syncwarp();
+            }
         }
-        if (lane == 0) {
-            size[survivor] = sa + sb;
-            sal[absorbed] = __longlong_as_double((long long)kd[e]);
-        }
-        __syncwarp();
     }
+    __syncthreads();
 }
 
-// ---------------------------------------------------------------- top-k + CSR
-// Row i: {j < sink} U {max(0,i-r)..i} U {topk blocks j <= i by (salience desc, j asc)}.
-struct TopkSmem {
-    unsigned long long *ok1, *ok2;  // sort keys: ~salience bits, j
-    int *order;                     // blocks by (salience desc, j asc)
-    int *cnt;                       // per-row counts, then row starts
-    unsigned *bm;                   // one bitmap of `words` words per warp
-};
-
-__device__ void row_bitmap(const TopkSmem &s, unsigned *bm, int words, int nb, int i, int sink,
+// Bitmap of row i in `bm` (one warp): sink range, local window, and the first topk blocks
+// j <= i of `order` (salience descending, index ascending).
+__device__ void row_bitmap(const int *order, unsigned *bm, int words, int nb, int i, int sink,
                            int r, int topk) {
     const int lane = threadIdx.x & 31;
     const int s_end = min(sink, i + 1);           // sink blocks [0, s_end)
@@ -487,14 +701,12 @@ __device__ void row_bitmap(const TopkSmem &s, unsigned *bm, int words, int nb, i
     for (int w = lane; w < words; w += 32) {
         const int lo = w * 32;
         unsigned m = 0;
-        // bits [lo, lo+32) intersected with [0, s_end)
         if (s_end > lo) m |= (s_end - lo >= 32) ? 0xFFFFFFFFu : ((1u << (s_end - lo)) - 1u);
-        // intersected with [l_beg, i]
-        const int a = max(l_beg, lo), b = min(i, lo + 31);
-        if (a <= b) {
-            const int n = b - a + 1;
+        const int x = max(l_beg, lo), y = min(i, lo + 31);
+        if (x <= y) {
+            const int n = y - x + 1;
             const unsigned run = (n >= 32) ? 0xFFFFFFFFu : ((1u << n) - 1u);
-            m |= run << (a - lo);
+            m |= run << (x - lo);
         }
         bm[w] = m;
     }
@@ -502,7 +714,7 @@ __device__ void row_bitmap(const TopkSmem &s, unsigned *bm, int words, int nb, i
     int need = min(topk, i + 1);
     for (int base = 0; need > 0 && base < nb; base += 32) {
         const int t = base + lane;
-        const int j = t < nb ? s.order[t] : INT_MAX;
+        const int j = t < nb ? order[t] : INT_MAX;
         const bool pred = j <= i;
         const unsigned bal = __ballot_sync(0xffffffffu, pred);
         const int rank = __popc(bal & ((1u << lane) - 1u));
@@ -512,90 +724,115 @@ __device__ void row_bitmap(const TopkSmem &s, unsigned *bm, int words, int nb, i
     __syncwarp();
 }
 
-__global__ void __launch_bounds__(1024) topk_csr(const double *__restrict__ sal, int nb, int pow2,
-                                                 int sink, int r, int topk,
-                                                 int32_t *__restrict__ row_ptr,
-                                                 int32_t *__restrict__ col_idx, int64_t col_cap,
-                                                 DeviceFlags flags) {
+__global__ void __launch_bounds__(512) schedule_graph_kernel(GraphArgs a) {
     extern __shared__ __align__(16) uint8_t sm[];
+    const int nb = a.nb;
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nt >> 5;
+    const int gwarp = blockIdx.x * nwarps + warp, gwarps = gridDim.x * nwarps;
+    // exchange buffer of the register sorts: 2 x blockDim 64-bit words after the phase areas
+    unsigned long long *xs = reinterpret_cast<unsigned long long *>(sm + a.xs_offset);
+    // ---- Boruvka: labels per CTA in shared memory, vertex bests double-buffered by round
+    int *scomp = reinterpret_cast<int *>(sm + (size_t)nb * 20);
+    for (int v = tid; v < nb; v += nt) scomp[v] = v;
+    if (blockIdx.x == 0 && tid == 0) a.counters[2] = 0;
+    __syncthreads();
+    int ncomp = nb, n_edges = 0;
+    for (int round = 0; round < a.rounds && ncomp > 1; ++round) {
+        double *vb_d = a.vb_d + (round & 1) * nb;
+        int *vb_u = a.vb_u + (round & 1) * nb;
+        vertex_min_phase(a, scomp, vb_d, vb_u);
+        if (!grid_sync(a.gbar, a.flags)) return;
+        ncomp = merge_phase(a, sm, scomp, vb_d, vb_u, &n_edges);
+    }
+    // ---- elder rule (CTA 0 holds the MST edges it recorded)
+    if (blockIdx.x == 0) elder_phase(a, sm, n_edges, xs);
+    if (!grid_sync(a.gbar, a.flags)) return;
+    // ---- top-k + CSR: every CTA sorts its own copy of the order
+    const int pow2 = a.pow2;
     const int words = (nb + 31) / 32;
-    const int nwarps = blockDim.x >> 5;
-    TopkSmem s;
-    s.ok1 = reinterpret_cast<unsigned long long *>(sm);
-    s.ok2 = s.ok1 + pow2;
-    s.order = reinterpret_cast<int *>(s.ok2 + pow2);
-    s.cnt = s.order + pow2;
-    s.bm = reinterpret_cast<unsigned *>(s.cnt + nb + 1);
-    __shared__ int warp_tot[32];
-    __shared__ int s_total;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < pow2; i += blockDim.x) {
+    unsigned long long *ok1 = reinterpret_cast<unsigned long long *>(sm);
+    unsigned long long *ok2 = ok1 + pow2;
+    int *order = reinterpret_cast<int *>(ok2 + pow2);
+    unsigned *bm = reinterpret_cast<unsigned *>(order + pow2) + warp * words;
+    for (int i = tid; i < pow2; i += nt) {
         if (i < nb) {
-            s.ok1[i] = ~(unsigned long long)__double_as_longlong(sal[i]);  // salience >= 0
-            s.ok2[i] = (unsigned long long)i;
+            ok1[i] = ~(unsigned long long)__double_as_longlong(
+                *reinterpret_cast<volatile double *>(&a.sal[i]));  // salience >= 0
+            ok2[i] = (unsigned long long)i;
         } else {
-            s.ok1[i] = ~0ull;
-            s.ok2[i] = ~0ull;
+            ok1[i] = ~0ull;
+            ok2[i] = ~0ull;
         }
     }
     __syncthreads();
-    bitonic_sort_pairs(s.ok1, s.ok2, pow2);
-    for (int i = tid; i < nb; i += blockDim.x) s.order[i] = (int)s.ok2[i];
+    if (pow2 <= nt) {
+        unsigned long long k1 = tid < pow2 ? ok1[tid] : ~0ull;
+        unsigned long long k2 = tid < pow2 ? ok2[tid] : ~0ull;
+        __syncthreads();
+        bitonic_sort_regs(k1, k2, xs);
+        if (tid < nb) order[tid] = (int)k2;
+    } else {
+        bitonic_sort_pairs(ok1, ok2, pow2);
+        for (int i = tid; i < nb; i += nt) order[i] = (int)ok2[i];
+    }
     __syncthreads();
-    unsigned *bm = s.bm + warp * words;
-    // counts
-    for (int i = warp; i < nb; i += nwarps) {
-        row_bitmap(s, bm, words, nb, i, sink, r, topk);
+    for (int i = gwarp; i < nb; i += gwarps) {
+        row_bitmap(order, bm, words, nb, i, a.sink, a.r, a.topk);
         int c = 0;
         for (int w = lane; w < words; w += 32) c += __popc(bm[w]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xffffffffu, c, off);
-        if (lane == 0) s.cnt[i] = c;
+        if (lane == 0) a.cnt[i] = c;
         __syncwarp();
     }
-    __syncthreads();
-    // exclusive scan of the counts (each thread a contiguous run)
-    const int per = (nb + blockDim.x - 1) / blockDim.x;
-    const int beg = min(nb, tid * per), end = min(nb, beg + per);
-    int run = 0;
-    for (int i = beg; i < end; ++i) run += s.cnt[i];
-    int incl = run;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) warp_tot[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int t = lane < nwarps ? warp_tot[lane] : 0;
+    if (!grid_sync(a.gbar, a.flags)) return;
+    if (blockIdx.x == 0) {
+        // exclusive scan of the counts: each thread a contiguous run, then warp / CTA totals
+        __shared__ int warp_tot[32];
+        const int per = (nb + nt - 1) / nt;
+        const int beg = min(nb, tid * per), end = min(nb, beg + per);
+        int run = 0;
+        for (int i = beg; i < end; ++i) run += a.cnt[i];
+        int incl = run;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, t, off);
-            if (lane >= off) t += o;
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
         }
-        warp_tot[lane] = t;  // inclusive over warps
-        if (lane == 31) s_total = t;
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int t = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, t, off);
+                if (lane >= off) t += o;
+            }
+            warp_tot[lane] = t;
+        }
+        __syncthreads();
+        int start = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - run;
+        for (int i = beg; i < end; ++i) {
+            const int c = a.cnt[i];
+            a.cnt[i] = start;
+            a.row_ptr[i] = start;
+            start += c;
+        }
+        if (tid == 0) {
+            const int total = warp_tot[nwarps - 1];
+            a.row_ptr[nb] = total;
+            if ((int64_t)total > a.col_cap) {
+                a.counters[2] = 1;
+                raise_status(a.flags, kDevCapacity);
+            }
+        }
     }
-    __syncthreads();
-    int start = (warp > 0 ? warp_tot[warp - 1] : 0) + incl - run;
-    __syncthreads();
-    for (int i = beg; i < end; ++i) {
-        const int c = s.cnt[i];
-        s.cnt[i] = start;
-        row_ptr[i] = start;
-        start += c;
-    }
-    if (tid == 0) row_ptr[nb] = s_total;
-    __syncthreads();
-    if ((int64_t)s_total > col_cap) {
-        if (tid == 0) raise_status(flags, kDevCapacity);
-        return;
-    }
-    // fill
-    for (int i = warp; i < nb; i += nwarps) {
-        row_bitmap(s, bm, words, nb, i, sink, r, topk);
-        int off = s.cnt[i];
+    if (!grid_sync(a.gbar, a.flags)) return;
+    if (*reinterpret_cast<volatile int *>(&a.counters[2]) != 0) return;
+    for (int i = gwarp; i < nb; i += gwarps) {
+        row_bitmap(order, bm, words, nb, i, a.sink, a.r, a.topk);
+        int off = *reinterpret_cast<volatile int *>(&a.cnt[i]);
         for (int w0 = 0; w0 < words; w0 += 32) {
             const int w = w0 + lane;
             unsigned bits = w < words ? bm[w] : 0u;
@@ -609,7 +846,7 @@ __global__ void __launch_bounds__(1024) topk_csr(const double *__restrict__ sal,
             int pos = off + inc - c;
             while (bits) {
                 const int bit = __ffs(bits) - 1;
-                col_idx[pos++] = w * 32 + bit;
+                a.col_idx[pos++] = w * 32 + bit;
                 bits &= bits - 1u;
             }
             off += __shfl_sync(0xffffffffu, inc, 31);
@@ -660,13 +897,15 @@ ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D
     w.cent = take(sizeof(double) * (size_t)(nb * D));
     w.d2 = take(sizeof(double) * (size_t)(nb * nb));
     w.comp = take(sizeof(int) * (size_t)nb);
-    w.vb_d = take(sizeof(double) * (size_t)nb);
-    w.vb_u = take(sizeof(int) * (size_t)nb);
+    w.vb_d = take(sizeof(double) * (size_t)(2 * nb));
+    w.vb_u = take(sizeof(int) * (size_t)(2 * nb));
     w.mst_d = take(sizeof(double) * (size_t)nb);
     w.mst_u = take(sizeof(int) * (size_t)nb);
     w.mst_v = take(sizeof(int) * (size_t)nb);
     w.counters = take(sizeof(int) * 4);
     w.sal = take(sizeof(double) * (size_t)nb);
+    w.cnt = take(sizeof(int) * (size_t)(nb + 1));
+    w.gbar = take(sizeof(unsigned) * 4);
     w.total = o;
     return w;
 }
@@ -713,27 +952,61 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
         const int t = (nb + kPdTile - 1) / kPdTile;
         pairwise_d2<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(cent, a.nb, a.D, t, d2);
     }
-    // Boruvka MST
-    boruvka_init<<<(nb + 255) / 256, 256, 0, st>>>(comp, nb, counters);
+    // MST, elder rule and CSR in one cooperative launch
     int rounds = 0;
     while ((1 << rounds) < nb) ++rounds;
-    const size_t merge_smem = (size_t)nb * (8 + 8 + 4);
-    const bool merge_ok = set_smem(boruvka_merge, 96 * 1024);
     const int pow2 = next_pow2(nb);
-    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 8;
-    const bool elder_ok = set_smem(elder_salience, 160 * 1024);
     const int words = (nb + 31) / 32;
-    const size_t topk_smem = (size_t)pow2 * 16 + (size_t)pow2 * 4 + (size_t)(nb + 1) * 4 + (size_t)32 * words * 4;
-    const bool topk_ok = set_smem(topk_csr, 200 * 1024);
-    if (!merge_ok || !elder_ok || !topk_ok) return TSA_ERR_CUDA;
-    for (int r = 0; r < rounds; ++r) {
-        boruvka_vertex_min<<<(nb + 7) / 8, 256, 0, st>>>(d2, comp, nb, counters, vb_d, vb_u);
-        boruvka_merge<<<1, 1024, merge_smem, st>>>(comp, nb, counters, vb_d, vb_u, mst_d, mst_u, mst_v);
-    }
-    // elder-rule salience, then the CSR
-    elder_salience<<<1, 1024, elder_smem, st>>>(nb, counters, mst_d, mst_u, mst_v, pow2, sal, a.flags);
-    topk_csr<<<1, 1024, topk_smem, st>>>(sal, nb, pow2, (int)a.sink, (int)a.local_radius, (int)a.topk,
-                                         a.row_ptr, a.col_idx, a.col_cap, a.flags);
+    constexpr int kGraphThreads = 512;
+    const size_t merge_smem = (size_t)nb * (8 + 8 + 4 + 4);
+    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 8;
+    const size_t topk_smem = (size_t)pow2 * 20 + (size_t)(kGraphThreads / 32) * words * 4;
+    size_t smem = merge_smem > elder_smem ? merge_smem : elder_smem;
+    if (topk_smem > smem) smem = topk_smem;
+    const size_t xs_offset = (smem + 15) & ~(size_t)15;
+    smem = xs_offset + (size_t)kGraphThreads * 16;
+    if (!set_smem(schedule_graph_kernel, smem)) return TSA_ERR_CUDA;
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, schedule_graph_kernel, kGraphThreads, smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return TSA_ERR_CUDA;
+    // one warp per vertex in the parallel phases is plenty; fewer CTAs make cheaper barriers
+    int ggrid = (nb + kGraphThreads / 32 - 1) / (kGraphThreads / 32);
+    if (ggrid > sms * per_sm) ggrid = sms * per_sm;
+    if (ggrid > sms) ggrid = sms;
+    if (ggrid < 1) ggrid = 1;
+    unsigned *gbar = reinterpret_cast<unsigned *>(w + ws.gbar);
+    if (cudaMemsetAsync(gbar, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return TSA_ERR_CUDA;
+    GraphArgs g;
+    g.d2 = d2;
+    g.nb = nb;
+    g.pow2 = pow2;
+    g.sink = (int)a.sink;
+    g.r = (int)a.local_radius;
+    g.topk = (int)a.topk;
+    g.rounds = rounds;
+    g.xs_offset = xs_offset;
+    g.comp = comp;
+    g.vb_d = vb_d;
+    g.vb_u = vb_u;
+    g.mst_d = mst_d;
+    g.mst_u = mst_u;
+    g.mst_v = mst_v;
+    g.counters = counters;
+    g.gbar = gbar;
+    g.sal = sal;
+    g.cnt = reinterpret_cast<int *>(w + ws.cnt);
+    g.row_ptr = a.row_ptr;
+    g.col_idx = a.col_idx;
+    g.col_cap = a.col_cap;
+    g.flags = a.flags;
+    void *args[] = {&g};
+    if (cudaLaunchCooperativeKernel((const void *)schedule_graph_kernel, dim3((unsigned)ggrid),
+                                    dim3(kGraphThreads), args, smem, st) != cudaSuccess)
+        return TSA_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }
 
