@@ -20,7 +20,6 @@ import csv
 import hashlib
 import io
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -65,6 +64,24 @@ def dist_env():
 
 def visited_flops(nnz: int, lanes: int, D: int, block: int = 64) -> float:
     return float(nnz) * lanes * 4.0 * block * block * D
+
+
+def aggregate_over_ranks(elapsed_ms: float, flops: float, device, world: int):
+    """Whole-job timing: the slowest rank's time and the sum of all ranks' work."""
+    if world <= 1:
+        return elapsed_ms, flops
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    w = torch.tensor([flops], device=device, dtype=torch.float64)
+    dist.all_reduce(w, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(w.item())
+
+
+def launches_per_step(topology: bool) -> int:
+    """Kernels of this library per step: centroid_partial, centroid_final, pairwise_d2 and
+    the cooperative graph kernel when the schedule is built, plus the attention kernel."""
+    return 1 + (4 if topology else 0)
 
 
 def dtype_name(dt) -> str:
@@ -215,7 +232,7 @@ def run_gpu(args):
         raise RuntimeError(f"device status {tsa.STATUS_NAMES.get(status, status)}")
     nnz = int(row_ptr[-1].item())
     flops = visited_flops(nnz, w.lanes, w.D, w.block)
-    launches_per_step = 1 + (6 + 2 * math.ceil(math.log2(w.nb)) if topo else 0)
+    n_launch = launches_per_step(topo)
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
@@ -247,15 +264,7 @@ def run_gpu(args):
     elapsed_ms = t0.elapsed_time(t1)
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     build_ms = [a.elapsed_time(b) for a, b in build_ev] if topo else [0.0]
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        tot = torch.tensor([flops], device=dev, dtype=torch.float64)
-        dist.all_reduce(tot, op=dist.ReduceOp.SUM)
-        flops_all = float(tot.item())
-    else:
-        flops_all = flops
+    elapsed_ms, flops_all = aggregate_over_ranks(elapsed_ms, flops, dev, world)
     ms_per_step = elapsed_ms / args.steps
     value = flops_all * args.steps / (elapsed_ms * 1e-3) / 1e12
 
@@ -310,7 +319,7 @@ def run_gpu(args):
             "peak_source": f"{peak_kind} bf16_tflops_sustained (cuBLAS bf16, seconds-long loop)",
             "traffic": traffic,
         },
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": n_launch * args.steps,
         "clocks": clk,
         "e2e": e2e,
     }
