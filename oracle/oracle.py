@@ -60,8 +60,10 @@ def lib():
         if _LIB is None:
             L = ctypes.CDLL(build())
             for name in ("oracle_decode", "oracle_dense_causal_csr", "oracle_centroids",
-                         "oracle_pairwise_d2", "oracle_salience", "oracle_topology_csr",
-                         "oracle_build_schedule", "oracle_attention"):
+                         "oracle_pairwise_d2", "oracle_salience", "oracle_salience_content",
+                         "oracle_topology_csr", "oracle_build_schedule",
+                         "oracle_build_schedule_tie", "oracle_segment_csr",
+                         "oracle_fixed_segment_csr", "oracle_attention"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -133,15 +135,19 @@ def pairwise_d2(C: np.ndarray) -> np.ndarray:
     return out
 
 
-def salience(C: np.ndarray):
-    """Elder-rule squared merge distance per block, plus the MST edges in Kruskal order."""
+def salience(C: np.ndarray, tie: str = "index"):
+    """Elder-rule squared merge distance per block, plus the MST edges in Kruskal order.
+
+    ``tie`` is "index" (ties broken by block index) or "content" (by centroid content).
+    """
+    fn = {"index": "oracle_salience", "content": "oracle_salience_content"}[tie]
     C = np.ascontiguousarray(C, dtype=np.float64)
     nb, D = C.shape
     sal = np.empty(nb, dtype=np.float64)
     mu = np.empty(max(nb - 1, 1), dtype=np.int32)
     mv = np.empty(max(nb - 1, 1), dtype=np.int32)
     md = np.empty(max(nb - 1, 1), dtype=np.float64)
-    _check(lib().oracle_salience(_p(C), _I64(nb), _I64(D), _p(sal), _p(mu), _p(mv), _p(md)),
+    _check(getattr(lib(), fn)(_p(C), _I64(nb), _I64(D), _p(sal), _p(mu), _p(mv), _p(md)),
            "salience")
     n = nb - 1
     return sal, (mu[:n], mv[:n], md[:n])
@@ -166,8 +172,9 @@ def topology_csr(sal_sq: np.ndarray, sink: int, local_radius: int, topk: int):
 
 
 def build_schedule(K, block: int, sink: int, local_radius: int, topk: int,
-                   dtype: int | None = None):
+                   dtype: int | None = None, tie: str = "index"):
     """Centroids -> elder-rule salience -> topology CSR. Returns (row_ptr, col_idx, sal_sq)."""
+    content = {"index": 0, "content": 1}[tie]
     bits, dt = _bits(K, dtype)
     if bits.ndim == 2:
         bits = bits[None]
@@ -178,11 +185,36 @@ def build_schedule(K, block: int, sink: int, local_radius: int, topk: int,
     row_ptr = np.empty(nb + 1, dtype=np.int32)
     col_idx = np.empty(cap, dtype=np.int32)
     sal = np.empty(nb, dtype=np.float64)
-    _check(lib().oracle_build_schedule(_p(bits), ctypes.c_int(dt), _I64(L), _I64(S), _I64(D),
-                                       _I64(block), _I64(sink), _I64(local_radius), _I64(topk),
-                                       _p(row_ptr), _p(col_idx), _I64(cap), _p(sal)),
+    _check(lib().oracle_build_schedule_tie(_p(bits), ctypes.c_int(dt), _I64(L), _I64(S), _I64(D),
+                                           _I64(block), _I64(sink), _I64(local_radius), _I64(topk),
+                                           ctypes.c_int(content), _p(row_ptr), _p(col_idx),
+                                           _I64(cap), _p(sal)),
            "build_schedule")
     return row_ptr, col_idx[: row_ptr[-1]].copy(), sal
+
+
+def segment_csr(S: int, block: int, starts):
+    """Block schedule of the segment mask whose segments begin at the tokens in ``starts``
+    (strictly ascending in [0, S); token 0 always begins one)."""
+    st = np.ascontiguousarray(np.asarray(starts, dtype=np.int64).reshape(-1))
+    nb = S // block
+    cap = max(nb * (nb + 1) // 2, 1)
+    row_ptr = np.empty(nb + 1, dtype=np.int32)
+    col_idx = np.empty(cap, dtype=np.int32)
+    _check(lib().oracle_segment_csr(_I64(S), _I64(block), _p(st), _I64(st.size), _p(row_ptr),
+                                    _p(col_idx), _I64(cap)), "segment_csr")
+    return row_ptr, col_idx[: row_ptr[-1]].copy()
+
+
+def fixed_segment_csr(S: int, block: int, seg_tokens: int):
+    """Block schedule of fixed segments of ``seg_tokens`` tokens."""
+    nb = S // block
+    cap = max(nb * (nb + 1) // 2, 1)
+    row_ptr = np.empty(nb + 1, dtype=np.int32)
+    col_idx = np.empty(cap, dtype=np.int32)
+    _check(lib().oracle_fixed_segment_csr(_I64(S), _I64(block), _I64(seg_tokens), _p(row_ptr),
+                                          _p(col_idx), _I64(cap)), "fixed_segment_csr")
+    return row_ptr, col_idx[: row_ptr[-1]].copy()
 
 
 def attention(Q, K, V, row_ptr, col_idx, block: int, scale: float, lanes=None, tokens=None,

@@ -23,6 +23,11 @@
  *        absorbed component depends on index order.
  *   [SCHED] the same mirror page, the world-model commit's schedule.py bullet:
  *        the block salience is reproduced from MST edges instead of all pairs.
+ *   [GATE] the same mirror page, the later commit about a forget gate's exact
+ *        zeros feeding the merged CSR kernel: segment boundaries as a CSR
+ *        schedule, with block counts at S 4096 and block 64 of 2,080 (dense),
+ *        288 (fixed 512-token segments), 160 (fixed 256-token segments) and
+ *        478 (random boundaries at 0.0024 flags per token, mean of 200 draws).
  *
  * Where the pages leave a step open, the reading taken is stated at the step.
  * All floating point is IEEE binary64; compile with -ffp-contract=off so that
@@ -183,18 +188,54 @@ int oracle_pairwise_d2(const double *C, int64_t nb, int64_t D, double *D2)
 
 typedef struct {
     double d2;
-    int32_t u, v; /* u < v */
+    int32_t u, v; /* u before v in the block order below */
 } edge_t;
 
-/* Reading: edges are ordered strictly by (d2, smaller index, larger index). */
+/*
+ * Block order used to break ties.
+ *
+ * Index rule ([PORT]: on a size tie the absorbed component "depends on index
+ * order"): blocks compare by index.
+ *
+ * Content rule (the fix the port note asks for: a tie-break on centroid
+ * content rather than index).  Reading: blocks compare by their centroid
+ * vectors, coordinate by coordinate in ascending d, each coordinate in IEEE
+ * 754 totalOrder (for finite values: numeric order, with -0 before +0); only
+ * blocks with bit-identical centroids fall back to index order.  The oracle
+ * requires finite centroids.
+ */
+static const double *g_order_C; /* qsort has no context argument */
+static int64_t g_order_D;
+static int g_order_content;
+
+static int coord_cmp(double x, double y)
+{
+    if (x < y) return -1;
+    if (x > y) return 1;
+    if (signbit(x) != signbit(y)) return signbit(x) ? -1 : 1;
+    return 0;
+}
+
+static int block_cmp(int32_t u, int32_t v)
+{
+    if (g_order_content) {
+        for (int64_t d = 0; d < g_order_D; ++d) {
+            int c = coord_cmp(g_order_C[u * g_order_D + d], g_order_C[v * g_order_D + d]);
+            if (c != 0) return c;
+        }
+    }
+    return u < v ? -1 : (u > v ? 1 : 0);
+}
+
+/* Reading: edges are ordered strictly by (d2, earlier endpoint, later endpoint). */
 static int edge_cmp(const void *pa, const void *pb)
 {
     const edge_t *a = (const edge_t *)pa, *b = (const edge_t *)pb;
     if (a->d2 < b->d2) return -1;
     if (a->d2 > b->d2) return 1;
-    if (a->u != b->u) return a->u < b->u ? -1 : 1;
-    if (a->v != b->v) return a->v < b->v ? -1 : 1;
-    return 0;
+    int c = block_cmp(a->u, b->u);
+    if (c != 0) return c;
+    return block_cmp(a->v, b->v);
 }
 
 static int32_t dsu_find(int32_t *parent, int32_t x)
@@ -214,19 +255,22 @@ static int32_t dsu_find(int32_t *parent, int32_t x)
  *
  * Kruskal over all nb(nb-1)/2 centroid pairs in the strict edge order.  Each
  * edge that joins two components merges them: the component with fewer blocks
- * is absorbed; on a size tie the component whose representative (root) has
- * the larger index is absorbed.  The absorbed component's root -- the one block
- * of that component never written before -- receives the edge's d2 as its
- * salience; the survivor's root stays the root of the union.  The block that is
- * never absorbed keeps salience 0.
+ * is absorbed; on a size tie the component whose representative (root) comes
+ * later in the block order is absorbed.  The absorbed component's root -- the
+ * one block of that component never written before -- receives the edge's d2
+ * as its salience; the survivor's root stays the root of the union.  The block
+ * that is never absorbed keeps salience 0.
  *
  * Outputs: sal_sq[nb] (squared merge distance per block) and, optionally, the
  * nb-1 accepted (MST) edges in the order they were accepted.
  */
-int oracle_salience(const double *C, int64_t nb, int64_t D, double *sal_sq,
-                    int32_t *mst_u, int32_t *mst_v, double *mst_d2)
+static int salience_kruskal(const double *C, int64_t nb, int64_t D, int content, double *sal_sq,
+                            int32_t *mst_u, int32_t *mst_v, double *mst_d2)
 {
     if (nb <= 0) return 1;
+    g_order_C = C;
+    g_order_D = D;
+    g_order_content = content;
     int64_t ne = nb * (nb - 1) / 2;
     edge_t *edges = (edge_t *)malloc(sizeof(edge_t) * (size_t)(ne > 0 ? ne : 1));
     int32_t *parent = (int32_t *)malloc(sizeof(int32_t) * (size_t)nb);
@@ -236,8 +280,9 @@ int oracle_salience(const double *C, int64_t nb, int64_t D, double *sal_sq,
     for (int64_t u = 0; u < nb; ++u)
         for (int64_t v = u + 1; v < nb; ++v) {
             edges[e].d2 = pair_d2(C, D, u, v);
-            edges[e].u = (int32_t)u;
-            edges[e].v = (int32_t)v;
+            int before = block_cmp((int32_t)u, (int32_t)v) < 0;
+            edges[e].u = (int32_t)(before ? u : v);
+            edges[e].v = (int32_t)(before ? v : u);
             ++e;
         }
     qsort(edges, (size_t)ne, sizeof(edge_t), edge_cmp);
@@ -254,7 +299,8 @@ int oracle_salience(const double *C, int64_t nb, int64_t D, double *sal_sq,
         int32_t absorbed, survivor;
         if (size[ra] < size[rb]) { absorbed = ra; survivor = rb; }
         else if (size[rb] < size[ra]) { absorbed = rb; survivor = ra; }
-        else { absorbed = ra > rb ? ra : rb; survivor = ra > rb ? rb : ra; }
+        else if (block_cmp(ra, rb) > 0) { absorbed = ra; survivor = rb; }
+        else { absorbed = rb; survivor = ra; }
         sal_sq[absorbed] = edges[k].d2;
         parent[absorbed] = survivor;
         size[survivor] += size[absorbed];
@@ -267,6 +313,20 @@ int oracle_salience(const double *C, int64_t nb, int64_t D, double *sal_sq,
     free(parent);
     free(size);
     return 0;
+}
+
+/* Index rule: size ties and equal distances are broken by block index. */
+int oracle_salience(const double *C, int64_t nb, int64_t D, double *sal_sq,
+                    int32_t *mst_u, int32_t *mst_v, double *mst_d2)
+{
+    return salience_kruskal(C, nb, D, 0, sal_sq, mst_u, mst_v, mst_d2);
+}
+
+/* Content rule: the same ties are broken by centroid content (block order above). */
+int oracle_salience_content(const double *C, int64_t nb, int64_t D, double *sal_sq,
+                            int32_t *mst_u, int32_t *mst_v, double *mst_d2)
+{
+    return salience_kruskal(C, nb, D, 1, sal_sq, mst_u, mst_v, mst_d2);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -324,19 +384,87 @@ int oracle_topology_csr(const double *sal_sq, int64_t nb, int64_t sink, int64_t 
     return 0;
 }
 
-/* The whole builder: centroids -> salience -> topology CSR. */
-int oracle_build_schedule(const uint16_t *K, int dtype, int64_t L, int64_t S, int64_t D,
-                          int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
-                          int32_t *row_ptr, int32_t *col_idx, int64_t col_cap, double *sal_sq)
+/* The whole builder: centroids -> salience -> topology CSR.  content selects
+ * the tie rule of the salience (0: index, 1: centroid content). */
+int oracle_build_schedule_tie(const uint16_t *K, int dtype, int64_t L, int64_t S, int64_t D,
+                              int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
+                              int content, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                              double *sal_sq)
 {
     if (block <= 0 || S <= 0 || S % block != 0) return 1;
     int64_t nb = S / block;
     double *C = (double *)malloc(sizeof(double) * (size_t)(nb * D));
     if (!C) return 2;
     int rc = oracle_centroids(K, dtype, L, S, D, block, C);
-    if (rc == 0) rc = oracle_salience(C, nb, D, sal_sq, NULL, NULL, NULL);
+    if (rc == 0) rc = salience_kruskal(C, nb, D, content, sal_sq, NULL, NULL, NULL);
     if (rc == 0) rc = oracle_topology_csr(sal_sq, nb, sink, local_radius, topk, row_ptr, col_idx, col_cap);
     free(C);
+    return rc;
+}
+
+int oracle_build_schedule(const uint16_t *K, int dtype, int64_t L, int64_t S, int64_t D,
+                          int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
+                          int32_t *row_ptr, int32_t *col_idx, int64_t col_cap, double *sal_sq)
+{
+    return oracle_build_schedule_tie(K, dtype, L, S, D, block, sink, local_radius, topk, 0,
+                                     row_ptr, col_idx, col_cap, sal_sq);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Segment schedules ([GATE]: segment boundaries run through the CSR kernel). */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Reading: `starts` lists the tokens that begin a new segment, strictly
+ * ascending in [0, S); token 0 always begins one.  Query token q may attend to
+ * key token k iff k <= q and no segment begins in (k, q], i.e. s(q) <= k <= q
+ * with s(q) the last segment start <= q.  Row i of the block schedule holds
+ * every key block that contains a key allowed to some query token of block i.
+ * When every start is a multiple of `block` the block schedule allows exactly
+ * the token pairs of the segment mask; otherwise it is the smallest block
+ * schedule that covers it.  Returns 3 if col_cap is too small.
+ */
+int oracle_segment_csr(int64_t S, int64_t block, const int64_t *starts, int64_t n_starts,
+                       int32_t *row_ptr, int32_t *col_idx, int64_t col_cap)
+{
+    if (S <= 0 || block <= 0 || S % block != 0 || n_starts < 0) return 1;
+    for (int64_t k = 0; k < n_starts; ++k) {
+        if (starts[k] < 0 || starts[k] >= S) return 1;
+        if (k > 0 && starts[k] <= starts[k - 1]) return 1;
+    }
+    int64_t nb = S / block;
+    unsigned char *mark = (unsigned char *)calloc((size_t)(nb * nb), 1);
+    if (!mark) return 2;
+    int64_t next = 0, seg = 0;
+    for (int64_t q = 0; q < S; ++q) {
+        while (next < n_starts && starts[next] <= q) seg = starts[next++];
+        for (int64_t k = seg; k <= q; ++k) mark[(q / block) * nb + k / block] = 1;
+    }
+    int64_t e = 0;
+    row_ptr[0] = 0;
+    for (int64_t i = 0; i < nb; ++i) {
+        for (int64_t j = 0; j < nb; ++j) {
+            if (!mark[i * nb + j]) continue;
+            if (e >= col_cap) { free(mark); return 3; }
+            col_idx[e++] = (int32_t)j;
+        }
+        row_ptr[i + 1] = (int32_t)e;
+    }
+    free(mark);
+    return 0;
+}
+
+/* Fixed segments of seg_tokens tokens: starts at seg_tokens, 2 seg_tokens, ... */
+int oracle_fixed_segment_csr(int64_t S, int64_t block, int64_t seg_tokens, int32_t *row_ptr,
+                             int32_t *col_idx, int64_t col_cap)
+{
+    if (seg_tokens <= 0 || S <= 0) return 1;
+    int64_t n = (S - 1) / seg_tokens;
+    int64_t *starts = (int64_t *)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    if (!starts) return 2;
+    for (int64_t k = 0; k < n; ++k) starts[k] = (k + 1) * seg_tokens;
+    int rc = oracle_segment_csr(S, block, starts, n, row_ptr, col_idx, col_cap);
+    free(starts);
     return rc;
 }
 
