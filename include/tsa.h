@@ -3,12 +3,15 @@
  *
  * Method: "Add topology-derived sparse attention kernel" (triton-lang/kernels#22),
  * Summary; and the port note on that PR's GitHub mirror page ("A port of the Triton
- * kernel merged as triton-lang/kernels#22").  Three operations:
+ * kernel merged as triton-lang/kernels#22").  The operations:
  *
  *   tsa_build_schedule      -- causal CSR block schedule from K: sink blocks, local-window
  *                              blocks and top-k blocks by 0D-persistence (elder-rule)
  *                              salience over key-block centroids.
  *   tsa_dense_causal_csr    -- the dense causal CSR (every block j <= i).
+ *   tsa_segment_csr         -- the CSR of a segment mask (fixed or listed segment starts).
+ *   tsa_build_schedule_ex   -- tsa_build_schedule with the elder rule's tie rule chosen
+ *                              (block index, or centroid content).
  *   tsa_scheduled_attention -- forward causal attention that visits, for each 64-token query
  *                              block, only the key blocks in its CSR row (online softmax,
  *                              token-level causal mask in the diagonal block).
@@ -105,6 +108,65 @@ tsa_status tsa_build_schedule(const void *K, tsa_dtype dtype, int64_t lanes, int
                               int64_t topk, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
                               double *salience_sq, void *workspace, size_t workspace_bytes,
                               tsa_stream_t stream);
+
+/*
+ * Tie rule of the elder rule.  TSA_TIE_INDEX is the rule above (ties on edge distance and on
+ * component size broken by block index).  TSA_TIE_CONTENT is the fix the mirror page's port
+ * note asks for (per-block salience is not permutation-equivariant because a size tie is broken
+ * by index; a fix needs a tie-break on centroid content): every tie the index rule breaks by
+ * index is broken by the centroid instead -- blocks compare lexicographically over d, each
+ * coordinate in IEEE 754 totalOrder (-0 before +0), and only bit-identical centroids fall back
+ * to the index.  Edges order by (d2, earlier endpoint, later endpoint) in that block order; on a
+ * size tie the root that comes later is absorbed.  Moving whole key blocks then moves each
+ * block's salience with it, bit for bit.  The top-k order (salience descending, lower j on
+ * ties) is the same under both rules.
+ */
+typedef enum { TSA_TIE_INDEX = 0, TSA_TIE_CONTENT = 1 } tsa_tie_break;
+
+/*
+ * tsa_build_schedule with an explicit tie rule (tsa_build_schedule is this call with
+ * TSA_TIE_INDEX).  Same arguments, workspace, limits and errors, plus INVALID_ARGUMENT for an
+ * unknown tie_break.  The result is bit-identical to the CPU oracle under the same rule.
+ */
+tsa_status tsa_build_schedule_ex(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S,
+                                 int64_t D, int64_t block, int64_t sink, int64_t local_radius,
+                                 int64_t topk, tsa_tie_break tie_break, int32_t *row_ptr,
+                                 int32_t *col_idx, int64_t col_cap, double *salience_sq,
+                                 void *workspace, size_t workspace_bytes, tsa_stream_t stream);
+
+/*
+ * Segment schedules ("Add topology-derived sparse attention kernel" mirror page, the later
+ * commit on a forget gate's exact zeros feeding the merged CSR kernel: a segment boundary is a
+ * CSR schedule the kernel runs with zero error; at S 4096, block 64 fixed 512-token segments
+ * visit 288 blocks and 256-token segments 160).
+ *
+ * Segments begin at token 0 and at each start.  Query token q may attend to key k iff
+ * s(q) <= k <= q, s(q) the last segment start <= q.  Row i holds every key block with a key
+ * allowed to some query of block i: the run s(block * i) / block .. i.  When every start is a
+ * multiple of `block`, attention over this CSR is exactly causal attention within each segment;
+ * otherwise the CSR is the smallest block schedule covering the segment mask, and the
+ * attention kernel lets tokens see across a boundary that falls inside a block.
+ *
+ * tsa_fixed_segment_nnz: nnz of fixed segments of segment_tokens tokens (starts at multiples of
+ *   segment_tokens); -1 for invalid arguments (S % block != 0, non-positive sizes, nb > 65534).
+ * tsa_fixed_segment_csr: that CSR.  col_cap >= tsa_fixed_segment_nnz(...), else CAPACITY.
+ * tsa_segment_csr: `starts` is a DEVICE array of n_starts int32 tokens, strictly ascending in
+ *   [0, S) (n_starts may be 0: one segment, the dense causal CSR).  Only the longest valid
+ *   prefix of `starts` is used; an entry out of order or range sets BAD_SCHEDULE in the device
+ *   status word.  nnz is at most nb(nb+1)/2; if it exceeds col_cap the rows are cut to fit and
+ *   the status word reports TSA_ERR_DEVICE.
+ *
+ *   row_ptr out, nb + 1 int32;  col_idx out, col_cap int32.
+ * Limits: S % block == 0, nb <= 65534, S < 2^31.  Errors: INVALID_ARGUMENT, CAPACITY,
+ * NOT_DEVICE_POINTER, DEVICE_MISMATCH, CUDA.
+ */
+int64_t tsa_fixed_segment_nnz(int64_t S, int64_t block, int64_t segment_tokens);
+tsa_status tsa_fixed_segment_csr(int64_t S, int64_t block, int64_t segment_tokens,
+                                 int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                                 tsa_stream_t stream);
+tsa_status tsa_segment_csr(int64_t S, int64_t block, const int32_t *starts, int64_t n_starts,
+                           int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                           tsa_stream_t stream);
 
 /*
  * Dense causal CSR ("Add topology-derived sparse attention kernel", Summary: "dense causal

@@ -21,7 +21,7 @@ def _declared():
 def test_every_declared_symbol_is_exported_and_bound():
     L = tsa.lib()
     names = _declared()
-    assert len(names) == 8
+    assert len(names) == 12
     for n in names:
         assert hasattr(L, n), n
         assert n in SIGNATURES, n
@@ -58,6 +58,13 @@ def test_host_checks_before_any_device_call():
     assert L.tsa_scheduled_attention(None, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 64, 0.1, None) == 1
     assert L.tsa_build_schedule(None, 0, 1, 64, 64, 64, 1, 1, 2, fake, fake, 10, None, fake, 1 << 20, None) == 1
     assert L.tsa_dense_causal_csr(64, 64, None, fake, 1, None) == 1
+    assert L.tsa_build_schedule_ex(fake, 0, 1, 64, 64, 64, 1, 1, 2, 7, fake, fake, 10, None, fake,
+                                   1 << 20, None) == 1  # unknown tie rule
+    assert L.tsa_fixed_segment_csr(4096, 64, 512, None, fake, 288, None) == 1
+    assert L.tsa_fixed_segment_csr(4096, 64, 512, fake, fake, 287, None) == 5  # capacity
+    assert L.tsa_fixed_segment_csr(4096, 64, 0, fake, fake, 288, None) == 1
+    assert L.tsa_segment_csr(4096, 64, None, 3, fake, fake, 10, None) == 1  # starts missing
+    assert L.tsa_segment_csr(4000, 64, None, 0, fake, fake, 10, None) == 1
     # unsupported block or head dimension
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 32, 0.1, None) == 2
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 96, 64, 0.1, None) == 2
@@ -79,3 +86,14 @@ def test_host_checks_before_any_device_call():
     # builder limits
     assert L.tsa_build_schedule(fake, 0, 1, 64 * 4097, 64, 64, 1, 1, 2, fake, fake, 1 << 30, None, fake,
                                 1 << 40, None) == 2
+
+
+def test_fixed_segment_nnz_closed_form():
+    # the mirror page's counts at S 4096, block 64: 288 (512-token), 160 (256-token), 2080 dense
+    assert tsa.tsa_fixed_segment_nnz(4096, 64, 512) == 288
+    assert tsa.tsa_fixed_segment_nnz(4096, 64, 256) == 160
+    assert tsa.tsa_fixed_segment_nnz(4096, 64, 4096) == 2080
+    assert tsa.tsa_fixed_segment_nnz(4096, 64, 64) == 64
+    assert tsa.tsa_fixed_segment_nnz(4096, 64, 1) == 64
+    assert tsa.tsa_fixed_segment_nnz(4000, 64, 512) == -1
+    assert tsa.tsa_fixed_segment_nnz(4096, 64, 0) == -1

@@ -22,6 +22,7 @@ STATUS_NAMES = {
     6: "TSA_ERR_CUDA", 7: "TSA_ERR_TIMEOUT", 8: "TSA_ERR_BAD_SCHEDULE", 9: "TSA_ERR_DEVICE",
 }
 TSA_F16, TSA_BF16 = 0, 1
+TIE_RULES = {"index": 0, "content": 1}
 
 _LOCK = threading.Lock()
 _LIB = None
@@ -37,8 +38,13 @@ SIGNATURES = {
     "tsa_build_schedule_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
     "tsa_build_schedule": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
                                           _P, _P, _I64, _P, _P, _SZ, _P]),
+    "tsa_build_schedule_ex": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                             ctypes.c_int, _P, _P, _I64, _P, _P, _SZ, _P]),
     "tsa_build_schedule_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64,
                                                   _I64, _P, _P, _I64, _P, _P]),
+    "tsa_fixed_segment_nnz": (_I64, [_I64, _I64, _I64]),
+    "tsa_fixed_segment_csr": (ctypes.c_int, [_I64, _I64, _I64, _P, _P, _I64, _P]),
+    "tsa_segment_csr": (ctypes.c_int, [_I64, _I64, _P, _I64, _P, _P, _I64, _P]),
     "tsa_dense_causal_csr": (ctypes.c_int, [_I64, _I64, _P, _P, _I64, _P]),
     "tsa_scheduled_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
                                                _I64, _I64, _I64, ctypes.c_float, _P]),
@@ -114,17 +120,20 @@ def tsa_build_schedule_workspace_bytes(lanes: int, S: int, D: int, block: int) -
 
 
 def tsa_build_schedule(K: torch.Tensor, block: int = 64, sink: int = 1, local_radius: int = 1,
-                       topk: int = 2, *, salience: bool = False, workspace: torch.Tensor | None = None,
-                       row_ptr: torch.Tensor | None = None, col_idx: torch.Tensor | None = None,
-                       stream=None):
+                       topk: int = 2, *, salience: bool = False, tie_break: str = "index",
+                       workspace: torch.Tensor | None = None, row_ptr: torch.Tensor | None = None,
+                       col_idx: torch.Tensor | None = None, stream=None):
     """Topology CSR from K ([S, D], [L, S, D] or [B, H, S, D]; lane-mean centroids).
 
-    Returns (row_ptr, col_idx) int32 device tensors -- col_idx has capacity length, its first
-    row_ptr[-1] entries are the schedule -- plus the per-block squared merge distance (float64)
-    when ``salience`` is true.
+    ``tie_break`` is "index" or "content" (the elder rule's tie rule).  Returns (row_ptr,
+    col_idx) int32 device tensors -- col_idx has capacity length, its first row_ptr[-1] entries
+    are the schedule -- plus the per-block squared merge distance (float64) when ``salience``
+    is true.
     """
     if not K.is_cuda or not K.is_contiguous():
         raise ValueError("K must be a contiguous CUDA tensor")
+    if tie_break not in TIE_RULES:
+        raise ValueError(f"tie_break must be one of {sorted(TIE_RULES)}")
     B, H, S, D = _lanes_S_D(K)
     lanes = B * H
     L = lib()
@@ -143,12 +152,52 @@ def tsa_build_schedule(K: torch.Tensor, block: int = 64, sink: int = 1, local_ra
     if col_idx is None:
         col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
     sal = torch.empty(nb, dtype=torch.float64, device=dev) if salience else None
-    _check(L.tsa_build_schedule(K.data_ptr(), _dtype_code(K), lanes, S, D, block, sink,
-                                local_radius, topk, row_ptr.data_ptr(), col_idx.data_ptr(),
-                                col_idx.numel(), sal.data_ptr() if sal is not None else None,
-                                workspace.data_ptr(), workspace.numel(), _stream(stream)),
-           "tsa_build_schedule")
+    _check(L.tsa_build_schedule_ex(K.data_ptr(), _dtype_code(K), lanes, S, D, block, sink,
+                                   local_radius, topk, TIE_RULES[tie_break], row_ptr.data_ptr(),
+                                   col_idx.data_ptr(), col_idx.numel(),
+                                   sal.data_ptr() if sal is not None else None,
+                                   workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "tsa_build_schedule_ex")
     return (row_ptr, col_idx, sal) if salience else (row_ptr, col_idx)
+
+
+def tsa_fixed_segment_nnz(S: int, block: int, segment_tokens: int) -> int:
+    return int(lib().tsa_fixed_segment_nnz(S, block, segment_tokens))
+
+
+def tsa_fixed_segment_csr(S: int, block: int, segment_tokens: int, device=None, stream=None):
+    """CSR of fixed segments of ``segment_tokens`` tokens, as int32 device tensors."""
+    nb = S // block if block > 0 else 0
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    nnz = tsa_fixed_segment_nnz(S, block, segment_tokens)
+    if nnz < 0:
+        raise TsaError(1, "tsa_fixed_segment_nnz")
+    row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+    col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=dev)
+    _check(lib().tsa_fixed_segment_csr(S, block, segment_tokens, row_ptr.data_ptr(),
+                                       col_idx.data_ptr(), col_idx.numel(), _stream(stream)),
+           "tsa_fixed_segment_csr")
+    return row_ptr, col_idx[:nnz]
+
+
+def tsa_segment_csr(S: int, block: int, starts: torch.Tensor, *, col_cap: int | None = None,
+                    stream=None):
+    """CSR of the segment mask whose segments begin at the int32 device tokens ``starts``.
+
+    col_idx has ``col_cap`` entries (default nb(nb+1)/2, always enough); the schedule is its
+    first row_ptr[-1] entries.
+    """
+    if starts.dtype != torch.int32 or not starts.is_cuda or not starts.is_contiguous():
+        raise TypeError("starts must be a contiguous int32 CUDA tensor")
+    nb = S // block if block > 0 else 0
+    if col_cap is None:
+        col_cap = max(nb * (nb + 1) // 2, 1)
+    row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=starts.device)
+    col_idx = torch.empty(col_cap, dtype=torch.int32, device=starts.device)
+    _check(lib().tsa_segment_csr(S, block, starts.data_ptr() if starts.numel() else None,
+                                 starts.numel(), row_ptr.data_ptr(), col_idx.data_ptr(), col_cap,
+                                 _stream(stream)), "tsa_segment_csr")
+    return row_ptr, col_idx
 
 
 def tsa_dense_causal_csr(S: int, block: int = 64, device=None, stream=None):

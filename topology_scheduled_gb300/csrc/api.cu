@@ -164,7 +164,18 @@ tsa_status tsa_build_schedule(const void *K, tsa_dtype dtype, int64_t lanes, int
                               int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
                               double *salience_sq, void *workspace, size_t workspace_bytes,
                               tsa_stream_t stream) {
+    return tsa_build_schedule_ex(K, dtype, lanes, S, D, block, sink, local_radius, topk, TSA_TIE_INDEX,
+                                 row_ptr, col_idx, col_cap, salience_sq, workspace, workspace_bytes,
+                                 stream);
+}
+
+tsa_status tsa_build_schedule_ex(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S, int64_t D,
+                                 int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
+                                 tsa_tie_break tie_break, int32_t *row_ptr, int32_t *col_idx,
+                                 int64_t col_cap, double *salience_sq, void *workspace,
+                                 size_t workspace_bytes, tsa_stream_t stream) {
     if (!K || !row_ptr || !col_idx || !workspace) return TSA_ERR_INVALID_ARGUMENT;
+    if (tie_break != TSA_TIE_INDEX && tie_break != TSA_TIE_CONTENT) return TSA_ERR_INVALID_ARGUMENT;
     if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
     if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
     if (sink < 0 || local_radius < 0 || topk < 0) return TSA_ERR_INVALID_ARGUMENT;
@@ -195,6 +206,7 @@ tsa_status tsa_build_schedule(const void *K, tsa_dtype dtype, int64_t lanes, int
     a.sink = sink < nb ? sink : nb;
     a.local_radius = local_radius < nb ? local_radius : nb;
     a.topk = topk < nb ? topk : nb;
+    a.content_ties = tie_break == TSA_TIE_CONTENT;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;
     a.col_cap = col_cap;
@@ -217,6 +229,48 @@ tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int3
     TSA_TRY(check_device_ptr(row_ptr, dev));
     TSA_TRY(check_device_ptr(col_idx, dev));
     return launch_dense_causal_csr(nb, row_ptr, col_idx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int64_t tsa_fixed_segment_nnz(int64_t S, int64_t block, int64_t segment_tokens) {
+    if (S <= 0 || block <= 0 || S % block != 0 || segment_tokens <= 0) return -1;
+    const int64_t nb = S / block;
+    if (nb > 65534) return -1;
+    int64_t total = 0;  // row i runs from the block of its segment start to i
+    for (int64_t i = 0; i < nb; ++i) total += i - ((i * block) / segment_tokens) * segment_tokens / block + 1;
+    return total;
+}
+
+tsa_status tsa_fixed_segment_csr(int64_t S, int64_t block, int64_t segment_tokens, int32_t *row_ptr,
+                                 int32_t *col_idx, int64_t col_cap, tsa_stream_t stream) {
+    if (!row_ptr || !col_idx) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t need = tsa_fixed_segment_nnz(S, block, segment_tokens);
+    if (need < 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (col_cap < need) return TSA_ERR_CAPACITY;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    TSA_TRY(check_device_ptr(row_ptr, dev));
+    TSA_TRY(check_device_ptr(col_idx, dev));
+    DeviceFlags flags;
+    TSA_TRY(device_flags(dev, &flags));
+    return launch_segment_csr(S, block, segment_tokens, nullptr, 0, row_ptr, col_idx, col_cap, flags,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+tsa_status tsa_segment_csr(int64_t S, int64_t block, const int32_t *starts, int64_t n_starts,
+                           int32_t *row_ptr, int32_t *col_idx, int64_t col_cap, tsa_stream_t stream) {
+    if (!row_ptr || !col_idx || (n_starts > 0 && !starts) || n_starts < 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (S <= 0 || block <= 0 || S % block != 0 || col_cap < 1) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = S / block;
+    if (nb > 65534 || S > INT_MAX) return TSA_ERR_INVALID_ARGUMENT;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    if (n_starts > 0) TSA_TRY(check_device_ptr(starts, dev));
+    TSA_TRY(check_device_ptr(row_ptr, dev));
+    TSA_TRY(check_device_ptr(col_idx, dev));
+    DeviceFlags flags;
+    TSA_TRY(device_flags(dev, &flags));
+    return launch_segment_csr(S, block, 0, n_starts > 0 ? starts : nullptr, n_starts, row_ptr, col_idx,
+                              col_cap, flags, reinterpret_cast<cudaStream_t>(stream));
 }
 
 tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,

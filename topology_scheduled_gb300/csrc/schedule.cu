@@ -276,6 +276,56 @@ __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, i
     }
 }
 
+// ---------------------------------------------------------------- content order
+// The content tie rule (the port note's fix for the index dependence of the elder rule) breaks
+// every tie by centroid content: blocks compare lexicographically over d, each coordinate in
+// IEEE 754 totalOrder, and only bit-identical centroids fall back to the index.  That order is
+// strict and total, so it ranks the blocks 0..nb-1.  Running the index-rule pipeline on the
+// centroids permuted into rank order applies exactly the content rule (every tie the index
+// rule breaks by index is then broken by rank), and the salience is written back through the
+// permutation.
+
+// totalOrder of binary64 as an unsigned key: negative values reversed below the positives.
+__device__ __forceinline__ unsigned long long total_order_key(double x) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+    return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
+}
+
+// One warp per block b: rank[b] = #{c : c before b}; perm[rank[b]] = b.
+__global__ void content_rank(const double *__restrict__ C, int64_t nb, int64_t D, int *__restrict__ perm) {
+    const int lane = threadIdx.x & 31;
+    const int64_t b = blockIdx.x * (int64_t)(blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (b >= nb) return;
+    const double *cb = C + b * D;
+    int count = 0;
+    for (int64_t c = lane; c < nb; c += 32) {
+        const double *cc = C + c * D;
+        int64_t d = 0;
+        unsigned long long kc = 0, kb = 0;
+        for (; d < D; ++d) {
+            kc = total_order_key(cc[d]);
+            kb = total_order_key(cb[d]);
+            if (kc != kb) break;
+        }
+        count += d < D ? (kc < kb) : (c < b);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) count += __shfl_xor_sync(0xffffffffu, count, off);
+    if (lane == 0) perm[count] = (int)b;
+}
+
+// Cp[r][:] = C[perm[r]][:]
+__global__ void permute_rows(const double *__restrict__ C, const int *__restrict__ perm, int64_t nb,
+                             int64_t D, double *__restrict__ Cp) {
+    const int64_t n = nb * D;
+    for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n;
+         w += (int64_t)gridDim.x * blockDim.x)
+    {
+        const int b = perm[w / D];
+        Cp[w] = (b >= 0 && b < nb) ? C[(int64_t)b * D + w % D] : 0.0;
+    }
+}
+
 // ---------------------------------------------------------------- pairwise distances
 constexpr int kPdTile = 16;   // pairs per tile side
 constexpr int kPdChunk = 32;  // d values staged per step
@@ -353,6 +403,7 @@ struct GraphArgs {
     int *counters;   // [0] components, [1] MST edges recorded, [2] CSR overflow
     unsigned *gbar;  // [0] arrivals, [1] generation, [2] gave up
     double *sal;
+    const int *perm; // content rule: block of each rank (the graph runs on ranks); else null
     int *cnt;        // per-row counts, then row starts
     int32_t *row_ptr, *col_idx;
     int64_t col_cap;
@@ -659,7 +710,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
                         sz[k] = (merge && owner && k == (survivor >> 5)) ? sx + sy : sz[k];
                     }
                     if (merge && lane == j)
-                        a.sal[absorbed] = __longlong_as_double((long long)my_d);
+                        a.sal[a.perm ? a.perm[absorbed] : absorbed] = __longlong_as_double((long long)my_d);
                 }
             }
         } else {
@@ -682,7 +733,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
                     if (label[v] == absorbed) label[v] = survivor;
                 if (lane == 0) {
                     size[survivor] = sx + sy;
-                    a.sal[absorbed] = __longlong_as_double((long long)kd[e]);
+                    a.sal[a.perm ? a.perm[absorbed] : absorbed] = __longlong_as_double((long long)kd[e]);
                 }
                 __syncwarp();
             }
@@ -905,6 +956,7 @@ ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D
     w.counters = take(sizeof(int) * 4);
     w.sal = take(sizeof(double) * (size_t)nb);
     w.cnt = take(sizeof(int) * (size_t)(nb + 1));
+    w.perm = take(sizeof(int) * (size_t)nb);
     w.gbar = take(sizeof(unsigned) * 4);
     w.total = o;
     return w;
@@ -947,10 +999,21 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
         const unsigned g = (unsigned)((n + 255) / 256);
         centroid_final<<<g, 256, 0, st>>>(part, a.lanes, a.nb, a.D, (double)(a.block * a.lanes), cent);
     }
+    // content rule: rank the blocks, run the graph on the centroids in rank order
+    int *perm = nullptr;
+    const double *graph_cent = cent;
+    if (a.content_ties) {
+        perm = reinterpret_cast<int *>(w + ws.perm);
+        content_rank<<<(unsigned)((a.nb + 7) / 8), 256, 0, st>>>(cent, a.nb, a.D, perm);
+        const int64_t n = a.nb * a.D;
+        permute_rows<<<(unsigned)((n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16), 256, 0, st>>>(
+            cent, perm, a.nb, a.D, part);
+        graph_cent = part;  // the per-lane sums are no longer needed
+    }
     // distances
     {
         const int t = (nb + kPdTile - 1) / kPdTile;
-        pairwise_d2<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(cent, a.nb, a.D, t, d2);
+        pairwise_d2<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(graph_cent, a.nb, a.D, t, d2);
     }
     // MST, elder rule and CSR in one cooperative launch
     int rounds = 0;
@@ -998,6 +1061,7 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
     g.counters = counters;
     g.gbar = gbar;
     g.sal = sal;
+    g.perm = perm;
     g.cnt = reinterpret_cast<int *>(w + ws.cnt);
     g.row_ptr = a.row_ptr;
     g.col_idx = a.col_idx;

@@ -37,7 +37,7 @@ constexpr int64_t kMaxScheduleDim = 1024;
 
 // Byte offsets of the builder's workspace regions (each 256-byte aligned).
 struct ScheduleWorkspace {
-    size_t part, cent, d2, comp, vb_d, vb_u, mst_d, mst_u, mst_v, counters, sal, cnt, gbar, total;
+    size_t part, cent, d2, comp, vb_d, vb_u, mst_d, mst_u, mst_v, counters, sal, cnt, perm, gbar, total;
 };
 ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D);
 
@@ -46,6 +46,7 @@ struct ScheduleLaunch {
     bool bf16;
     int64_t lanes, S, D, block, nb;
     int64_t sink, local_radius, topk;
+    bool content_ties;  // break ties by centroid content instead of block index
     int32_t *row_ptr, *col_idx;
     int64_t col_cap;
     double *salience_sq;  // may be null
@@ -57,5 +58,9 @@ struct ScheduleLaunch {
 tsa_status launch_build_schedule(const ScheduleLaunch &a);
 tsa_status launch_dense_causal_csr(int64_t nb, int32_t *row_ptr, int32_t *col_idx,
                                    cudaStream_t stream);
+// Segment schedule: fixed segments of seg_tokens (> 0), or the listed starts (seg_tokens 0).
+tsa_status launch_segment_csr(int64_t S, int64_t block, int64_t seg_tokens, const int32_t *starts,
+                              int64_t n_starts, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                              const DeviceFlags &flags, cudaStream_t stream);
 
 }  // namespace tsa
