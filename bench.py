@@ -1,7 +1,8 @@
 """Benchmark: one step = build the topology CSR from K, then scheduled attention over it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {tsa,reference}]
-                    [--workload NAME] [--schedule topology|dense|density:P]
+                    [--workload NAME]
+                    [--schedule topology|topology-content|segment:TOKENS|dense|density:P]
 
 Metric: scheduled-attention forward TFLOP/s counted on visited blocks
 (nnz * lanes * 4 * 64^2 * D per step) and ms per step.  Default workload: [B=2, H=32,
@@ -9,6 +10,10 @@ S=32768, D=128] bf16, block 64, sink 2, local_radius 4, topk 8, keys clustered o
 means (the S 32768 configuration).  Inputs are synthetic, seeded, resident in HBM and larger
 than L2 (no flush needed).  Under torchrun every rank runs its own independent problem
 (seed = rank): weak scaling, no collective on the data path.
+
+Schedules built on the GPU inside every step: "topology" (elder rule, index ties),
+"topology-content" (content ties), "segment:TOKENS" (fixed segments).  "dense" and
+"density:P" are built once before timing.
 
 --impl reference times the CPU oracle (oracle/, fp64) on the host cores on a bounded
 sample of the same workload.
@@ -78,10 +83,21 @@ def aggregate_over_ranks(elapsed_ms: float, flops: float, device, world: int):
     return float(t.item()), float(w.item())
 
 
-def launches_per_step(topology: bool) -> int:
-    """Kernels of this library per step: centroid_partial, centroid_final, pairwise_d2 and
-    the cooperative graph kernel when the schedule is built, plus the attention kernel."""
-    return 1 + (4 if topology else 0)
+def launches_per_step(schedule: str) -> int:
+    """Kernels of this library per step: the attention kernel, plus the builder's kernels when
+    the schedule is built inside the step -- centroid_partial, centroid_final, pairwise_d2 and
+    the cooperative graph kernel for a topology schedule (content_rank and permute_rows in
+    addition under content ties), segment_rows and segment_fill for fixed segments."""
+    return 1 + {"topology": 4, "topology-content": 6}.get(
+        schedule, 2 if schedule.startswith("segment:") else 0)
+
+
+def built_in_step(schedule: str) -> bool:
+    return schedule in ("topology", "topology-content") or schedule.startswith("segment:")
+
+
+def segment_tokens(schedule: str) -> int:
+    return int(schedule.split(":")[1])
 
 
 def dtype_name(dt) -> str:
@@ -183,6 +199,39 @@ def build_schedule_host(w, schedule: str):
     raise ValueError(schedule)
 
 
+def gpu_builder(schedule: str, w, tsa, k, ws):
+    """The schedule build that runs inside every step, as a call writing (row_ptr, col_idx);
+    called with no arguments it allocates them and returns them.  None for host-built CSRs."""
+    if schedule in ("topology", "topology-content"):
+        tie = "content" if schedule == "topology-content" else "index"
+        cap = tsa.tsa_schedule_max_nnz(w.S, w.block, w.sink, w.local_radius, w.topk)
+
+        def build(row_ptr=None, col_idx=None):
+            if row_ptr is None:
+                row_ptr = torch.empty(w.nb + 1, dtype=torch.int32, device=k.device)
+                col_idx = torch.empty(cap, dtype=torch.int32, device=k.device)
+            tsa.tsa_build_schedule(k, w.block, w.sink, w.local_radius, w.topk, tie_break=tie,
+                                   workspace=ws, row_ptr=row_ptr, col_idx=col_idx)
+            return row_ptr, col_idx
+        return build
+    if schedule.startswith("segment:"):
+        seg = segment_tokens(schedule)
+        nnz = tsa.tsa_fixed_segment_nnz(w.S, w.block, seg)
+        L = tsa.lib()
+
+        def build(row_ptr=None, col_idx=None):
+            if row_ptr is None:
+                row_ptr = torch.empty(w.nb + 1, dtype=torch.int32, device=k.device)
+                col_idx = torch.empty(max(nnz, 1), dtype=torch.int32, device=k.device)
+            st = L.tsa_fixed_segment_csr(w.S, w.block, seg, row_ptr.data_ptr(), col_idx.data_ptr(),
+                                         col_idx.numel(), torch.cuda.current_stream().cuda_stream)
+            if st != 0:
+                raise tsa.TsaError(st, "tsa_fixed_segment_csr")
+            return row_ptr, col_idx
+        return build
+    return None
+
+
 def run_gpu(args):
     import torch.distributed as dist
 
@@ -197,13 +246,12 @@ def run_gpu(args):
     stream = torch.cuda.current_stream()
     q, k, v = make_qkv(w, seed=rank, device=dev)
     out = torch.empty_like(q)
-    cap = tsa.tsa_schedule_max_nnz(w.S, w.block, w.sink, w.local_radius, w.topk)
     ws = torch.empty(tsa.tsa_build_schedule_workspace_bytes(w.lanes, w.S, w.D, w.block),
                      dtype=torch.uint8, device=dev)
-    topo = args.schedule == "topology"
+    topo = built_in_step(args.schedule)
+    build = gpu_builder(args.schedule, w, tsa, k, ws)
     if topo:
-        row_ptr = torch.empty(w.nb + 1, dtype=torch.int32, device=dev)
-        col_idx = torch.empty(cap, dtype=torch.int32, device=dev)
+        row_ptr, col_idx = build()
     elif args.schedule == "dense":
         row_ptr, col_idx = tsa.tsa_dense_causal_csr(w.S, w.block, device=dev)
     else:
@@ -216,8 +264,7 @@ def run_gpu(args):
         if topo:
             if build_events:
                 build_events[0].record(stream)
-            tsa.tsa_build_schedule(k, w.block, w.sink, w.local_radius, w.topk, workspace=ws,
-                                   row_ptr=row_ptr, col_idx=col_idx)
+            build(row_ptr, col_idx)
             if build_events:
                 build_events[1].record(stream)
         if attn_events:
@@ -232,7 +279,7 @@ def run_gpu(args):
         raise RuntimeError(f"device status {tsa.STATUS_NAMES.get(status, status)}")
     nnz = int(row_ptr[-1].item())
     flops = visited_flops(nnz, w.lanes, w.D, w.block)
-    n_launch = launches_per_step(topo)
+    n_launch = launches_per_step(args.schedule)
     for _ in range(max(args.warmup, 0)):
         step()
     torch.cuda.synchronize()
@@ -270,7 +317,7 @@ def run_gpu(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, tsa, q, k, v, out, ws, row_ptr, col_idx, topo, flops, stream, world)
+        e2e = run_e2e(args, w, tsa, q, k, v, out, build, row_ptr, col_idx, topo, flops, stream, world)
 
     peaks, peak_kind = measured_peaks()
     attn_mean = statistics.mean(attn_ms)
@@ -331,7 +378,7 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, tsa, q, k, v, out, ws, row_ptr, col_idx, topo, flops, stream, world):
+def run_e2e(args, w, tsa, q, k, v, out, build, row_ptr, col_idx, topo, flops, stream, world):
     """Same step through the public API from pinned host buffers, copies inside the timing."""
     steps = max(1, min(args.steps, 5))
     hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
@@ -343,8 +390,7 @@ def run_e2e(args, w, tsa, q, k, v, out, ws, row_ptr, col_idx, topo, flops, strea
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
         if topo:
-            tsa.tsa_build_schedule(k, w.block, w.sink, w.local_radius, w.topk, workspace=ws,
-                                   row_ptr=row_ptr, col_idx=col_idx)
+            build(row_ptr, col_idx)
         tsa.tsa_scheduled_attention(q, k, v, row_ptr, col_idx, w.scale, out=out)
         ho.copy_(out, non_blocking=True)
         hnnz.copy_(row_ptr[-1:], non_blocking=True)
@@ -373,8 +419,11 @@ def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo):
     S, D = w.S, w.D
     kh = k.reshape(-1, S, D)
     t0 = time.perf_counter()
-    if topo:
-        rp, ci, _ = oracle.build_schedule(kh, w.block, w.sink, w.local_radius, w.topk)
+    if args.schedule.startswith("segment:"):
+        rp, ci = oracle.fixed_segment_csr(S, w.block, segment_tokens(args.schedule))
+    elif topo:
+        tie = "content" if args.schedule == "topology-content" else "index"
+        rp, ci, _ = oracle.build_schedule(kh, w.block, w.sink, w.local_radius, w.topk, tie=tie)
     else:
         rp = row_ptr.cpu().numpy()
         ci = col_idx.cpu().numpy()[: rp[-1]]
@@ -410,7 +459,7 @@ def run_reference(args):
     if rank != 0:
         return
     w = workload(args)
-    topo = args.schedule == "topology"
+    topo = built_in_step(args.schedule)
     q, k, v = make_qkv(w, seed=0, device="cpu")
     if topo:
         rp = ci = None

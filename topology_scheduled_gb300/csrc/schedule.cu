@@ -404,6 +404,7 @@ struct GraphArgs {
     unsigned *gbar;  // [0] arrivals, [1] generation, [2] gave up
     double *sal;
     const int *perm; // content rule: block of each rank (the graph runs on ranks); else null
+    double *sal_rank; // content rule: salience by rank, before the scatter to blocks
     int *cnt;        // per-row counts, then row starts
     int32_t *row_ptr, *col_idx;
     int64_t col_cap;
@@ -644,6 +645,9 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     volatile int *size = reinterpret_cast<volatile int *>(kab + pow2);
     volatile int *label = size + nb;  // used only when nb > 32 * kLabelRegs
     const int ne = nb - 1;
+    // under content ties the merges run on ranks: salience goes to a rank-indexed scratch and
+    // is scattered to blocks at the end (one global write per merge, no dependent load)
+    double *sal = a.perm ? a.sal_rank : a.sal;
     if (threadIdx.x == 0 && n_edges != ne) raise_status(a.flags, kDevCapacity);
     for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
         if (i < ne) {
@@ -657,7 +661,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     for (int v = threadIdx.x; v < nb; v += blockDim.x) {
         label[v] = v;
         size[v] = 1;
-        a.sal[v] = 0.0;
+        sal[v] = 0.0;
     }
     __syncthreads();
     const bool fast = nb <= 32 * kLabelRegs && pow2 <= (int)blockDim.x;
@@ -710,7 +714,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
                         sz[k] = (merge && owner && k == (survivor >> 5)) ? sx + sy : sz[k];
                     }
                     if (merge && lane == j)
-                        a.sal[a.perm ? a.perm[absorbed] : absorbed] = __longlong_as_double((long long)my_d);
+                        sal[absorbed] = __longlong_as_double((long long)my_d);
                 }
             }
         } else {
@@ -733,13 +737,20 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
                     if (label[v] == absorbed) label[v] = survivor;
                 if (lane == 0) {
                     size[survivor] = sx + sy;
-                    a.sal[a.perm ? a.perm[absorbed] : absorbed] = __longlong_as_double((long long)kd[e]);
+                    sal[absorbed] = __longlong_as_double((long long)kd[e]);
                 }
                 __syncwarp();
             }
         }
     }
     __syncthreads();
+    if (a.perm) {
+        for (int r = threadIdx.x; r < nb; r += blockDim.x) {
+            const int b = a.perm[r];
+            if (b >= 0 && b < nb) a.sal[b] = sal[r];
+        }
+        __syncthreads();
+    }
 }
 
 // Bitmap of row i in `bm` (one warp): sink range, local window, and the first topk blocks
@@ -957,6 +968,7 @@ ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D
     w.sal = take(sizeof(double) * (size_t)nb);
     w.cnt = take(sizeof(int) * (size_t)(nb + 1));
     w.perm = take(sizeof(int) * (size_t)nb);
+    w.sal_rank = take(sizeof(double) * (size_t)nb);
     w.gbar = take(sizeof(unsigned) * 4);
     w.total = o;
     return w;
@@ -1062,6 +1074,7 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
     g.gbar = gbar;
     g.sal = sal;
     g.perm = perm;
+    g.sal_rank = reinterpret_cast<double *>(w + ws.sal_rank);
     g.cnt = reinterpret_cast<int *>(w + ws.cnt);
     g.row_ptr = a.row_ptr;
     g.col_idx = a.col_idx;
