@@ -63,7 +63,8 @@ def lib():
                          "oracle_pairwise_d2", "oracle_salience", "oracle_salience_content",
                          "oracle_topology_csr", "oracle_build_schedule",
                          "oracle_build_schedule_tie", "oracle_segment_csr",
-                         "oracle_fixed_segment_csr", "oracle_attention"):
+                         "oracle_fixed_segment_csr", "oracle_attention",
+                         "oracle_attention_lse", "oracle_attention_backward"):
                 getattr(L, name).restype = ctypes.c_int
             _LIB = L
     return _LIB
@@ -217,20 +218,32 @@ def fixed_segment_csr(S: int, block: int, seg_tokens: int):
     return row_ptr, col_idx[: row_ptr[-1]].copy()
 
 
+def _qkv_bits(tensors, dtype):
+    bits = [_bits(t, dtype) for t in tensors]
+    if len({b[1] for b in bits}) != 1:
+        raise TypeError("inputs must share a dtype")
+    S, D = bits[0][0].shape[-2], bits[0][0].shape[-1]
+    return [b[0].reshape(-1, S, D) for b in bits], bits[0][1], S, D
+
+
+def _csr(row_ptr, col_idx):
+    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
+    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
+    if col_idx.size == 0:
+        col_idx = np.zeros(1, dtype=np.int32)
+    return row_ptr, col_idx
+
+
 def attention(Q, K, V, row_ptr, col_idx, block: int, scale: float, lanes=None, tokens=None,
-              online: bool = False, nthreads: int = 1, dtype: int | None = None) -> np.ndarray:
+              online: bool = False, nthreads: int = 1, dtype: int | None = None,
+              return_lse: bool = False):
     """fp64 masked attention for chosen (lane, token) rows; all rows when lanes/tokens are None.
 
     Q, K, V are [L, S, D] or [S, D] (or [B, H, S, D]); returns [n, D] float64 (or the full
-    [L, S, D] array when no rows are given).
+    [L, S, D] array when no rows are given), and with ``return_lse`` also the log-sum-exp of
+    the scaled scores per row ([n] or [L, S]; -inf for a row without keys).
     """
-    qb, dt = _bits(Q, dtype)
-    kb, dk = _bits(K, dtype)
-    vb, dv = _bits(V, dtype)
-    if not (dt == dk == dv):
-        raise TypeError("Q, K, V must share a dtype")
-    S, D = qb.shape[-2], qb.shape[-1]
-    qb, kb, vb = (a.reshape(-1, S, D) for a in (qb, kb, vb))
+    (qb, kb, vb), dt, S, D = _qkv_bits((Q, K, V), dtype)
     L = qb.shape[0]
     full = lanes is None
     if full:
@@ -238,16 +251,31 @@ def attention(Q, K, V, row_ptr, col_idx, block: int, scale: float, lanes=None, t
         tokens = np.tile(np.arange(S, dtype=np.int64), L)
     lanes = np.ascontiguousarray(lanes, dtype=np.int64)
     tokens = np.ascontiguousarray(tokens, dtype=np.int64)
-    row_ptr = np.ascontiguousarray(row_ptr, dtype=np.int32)
-    col_idx = np.ascontiguousarray(col_idx, dtype=np.int32)
-    if col_idx.size == 0:
-        col_idx = np.zeros(1, dtype=np.int32)
+    row_ptr, col_idx = _csr(row_ptr, col_idx)
     out = np.empty((lanes.shape[0], D), dtype=np.float64)
-    _check(lib().oracle_attention(_p(qb), _p(kb), _p(vb), ctypes.c_int(dt), _I64(L), _I64(S),
-                                  _I64(D), _I64(block), ctypes.c_double(scale), _p(row_ptr),
-                                  _p(col_idx), _I64(lanes.shape[0]), _p(lanes), _p(tokens),
-                                  _p(out), ctypes.c_int(1 if online else 0),
-                                  ctypes.c_int(int(nthreads))), "attention")
+    lse = np.empty(lanes.shape[0], dtype=np.float64) if return_lse else None
+    _check(lib().oracle_attention_lse(_p(qb), _p(kb), _p(vb), ctypes.c_int(dt), _I64(L), _I64(S),
+                                      _I64(D), _I64(block), ctypes.c_double(scale), _p(row_ptr),
+                                      _p(col_idx), _I64(lanes.shape[0]), _p(lanes), _p(tokens),
+                                      _p(out), _p(lse) if lse is not None else None,
+                                      ctypes.c_int(1 if online else 0),
+                                      ctypes.c_int(int(nthreads))), "attention")
     if full:
-        return out.reshape(L, S, D)
-    return out
+        out = out.reshape(L, S, D)
+        lse = lse.reshape(L, S) if lse is not None else None
+    return (out, lse) if return_lse else out
+
+
+def attention_backward(Q, K, V, dO, row_ptr, col_idx, block: int, scale: float,
+                       nthreads: int = 1, dtype: int | None = None):
+    """fp64 gradients (dQ, dK, dV), each [L, S, D], of the masked attention for upstream dO."""
+    (qb, kb, vb, ob), dt, S, D = _qkv_bits((Q, K, V, dO), dtype)
+    L = qb.shape[0]
+    row_ptr, col_idx = _csr(row_ptr, col_idx)
+    grads = [np.empty((L, S, D), dtype=np.float64) for _ in range(3)]
+    _check(lib().oracle_attention_backward(_p(qb), _p(kb), _p(vb), _p(ob), ctypes.c_int(dt),
+                                           _I64(L), _I64(S), _I64(D), _I64(block),
+                                           ctypes.c_double(scale), _p(row_ptr), _p(col_idx),
+                                           _p(grads[0]), _p(grads[1]), _p(grads[2]),
+                                           ctypes.c_int(int(nthreads))), "attention_backward")
+    return tuple(grads)

@@ -491,12 +491,13 @@ typedef struct {
     const int32_t *row_ptr, *col_idx;
     const int64_t *lane, *tok;
     double *out;
+    double *lse; /* optional: log-sum-exp of the scaled scores per row */
     int online;
     int64_t begin, end;
 } attn_job_t;
 
 static void attention_one_twopass(const attn_job_t *J, int64_t l, int64_t q, double *o,
-                                  double *s, int64_t *keys)
+                                  double *s, int64_t *keys, double *lse)
 {
     const int64_t D = J->D, S = J->S, block = J->block;
     const double *tab = J->tab;
@@ -508,6 +509,7 @@ static void attention_one_twopass(const attn_job_t *J, int64_t l, int64_t q, dou
             if (k <= q) keys[n++] = k;
     }
     for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+    if (lse) *lse = -INFINITY;
     if (n == 0) return;
     double m = -INFINITY;
     for (int64_t a = 0; a < n; ++a) {
@@ -522,6 +524,7 @@ static void attention_one_twopass(const attn_job_t *J, int64_t l, int64_t q, dou
         s[a] = exp(s[a] - m);
         den += s[a];
     }
+    if (lse) *lse = m + log(den);
     for (int64_t a = 0; a < n; ++a) {
         const uint16_t *vrow = J->V + (l * S + keys[a]) * D;
         double w = s[a] / den;
@@ -584,7 +587,8 @@ static void *attention_worker(void *arg)
             if (J->online)
                 attention_one_online(J, J->lane[r], J->tok[r], o, s);
             else
-                attention_one_twopass(J, J->lane[r], J->tok[r], o, s, keys);
+                attention_one_twopass(J, J->lane[r], J->tok[r], o, s, keys,
+                                      J->lse ? J->lse + r : NULL);
         }
     }
     free(s);
@@ -596,13 +600,32 @@ static void *attention_worker(void *arg)
  * Evaluate O for n (lane, token) pairs.  Q, K, V are [L][S][D] 16-bit values of
  * the given dtype; out is [n][D] binary64.  Rows are independent, so they are
  * split into nthreads contiguous chunks; the result does not depend on nthreads.
+ * lse (optional, two-pass form only) receives log(sum_k exp(scale <Q_q, K_k>))
+ * over the allowed keys, -inf for a row without keys.
  */
+int oracle_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
+                         int64_t L, int64_t S, int64_t D, int64_t block, double scale,
+                         const int32_t *row_ptr, const int32_t *col_idx, int64_t n,
+                         const int64_t *lane, const int64_t *tok, double *out, double *lse,
+                         int online, int nthreads);
+
 int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
                      int64_t L, int64_t S, int64_t D, int64_t block, double scale,
                      const int32_t *row_ptr, const int32_t *col_idx, int64_t n,
                      const int64_t *lane, const int64_t *tok, double *out, int online,
                      int nthreads)
 {
+    return oracle_attention_lse(Q, K, V, dtype, L, S, D, block, scale, row_ptr, col_idx, n, lane,
+                                tok, out, NULL, online, nthreads);
+}
+
+int oracle_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int dtype,
+                         int64_t L, int64_t S, int64_t D, int64_t block, double scale,
+                         const int32_t *row_ptr, const int32_t *col_idx, int64_t n,
+                         const int64_t *lane, const int64_t *tok, double *out, double *lse,
+                         int online, int nthreads)
+{
+    if (lse && online) return 1;
     if (block <= 0 || S % block != 0 || L <= 0 || D <= 0) return 1;
     for (int64_t r = 0; r < n; ++r)
         if (lane[r] < 0 || lane[r] >= L || tok[r] < 0 || tok[r] >= S) return 1;
@@ -613,7 +636,7 @@ int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, in
     base.tab = decode_table(dtype);
     base.S = S; base.D = D; base.block = block; base.scale = scale;
     base.row_ptr = row_ptr; base.col_idx = col_idx;
-    base.lane = lane; base.tok = tok; base.out = out; base.online = online;
+    base.lane = lane; base.tok = tok; base.out = out; base.lse = lse; base.online = online;
     attn_job_t jobs[256];
     pthread_t th[256];
     int started[256];
@@ -630,6 +653,141 @@ int oracle_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, in
     for (int t = 1; t < nthreads; ++t) {
         if (started[t]) pthread_join(th[t], NULL);
         else if (jobs[t].begin < jobs[t].end) attention_worker(&jobs[t]);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Backward pass of the masked attention above (the step after the forward   */
+/* kernel; the mirror page's segment-boundary record notes that the merged   */
+/* kernel has none).  It is the chain rule of the forward definition, with   */
+/* the same allowed sets A(q).                                               */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * For lane l, with p_qk = softmax_k(scale <Q_q, K_k>) over k in A(q) and
+ * O_q = sum_k p_qk V_k, the gradients of a loss with dL/dO = dO are
+ *
+ *   dV_k  = sum_{q : k in A(q)} p_qk dO_q
+ *   dP_qk = <dO_q, V_k>,   Delta_q = <dO_q, O_q> = sum_k p_qk dP_qk
+ *   dS_qk = p_qk (dP_qk - Delta_q)
+ *   dQ_q  = scale sum_k dS_qk K_k,   dK_k = scale sum_{q : k in A(q)} dS_qk Q_q
+ *
+ * all in binary64 from the exactly widened 16-bit inputs.  A query without
+ * allowed keys contributes nothing.  Lanes are independent; each lane runs in
+ * one thread, queries in ascending order, so the result does not depend on
+ * nthreads.
+ */
+typedef struct {
+    const uint16_t *Q, *K, *V, *dO;
+    const double *tab;
+    int64_t S, D, block;
+    double scale;
+    const int32_t *row_ptr, *col_idx;
+    double *dQ, *dK, *dV;
+    int64_t lane_begin, lane_end;
+} bwd_job_t;
+
+static void backward_lane(const bwd_job_t *J, int64_t l, double *p, int64_t *keys, double *o)
+{
+    const int64_t S = J->S, D = J->D, block = J->block;
+    const double *tab = J->tab;
+    double *dQ = J->dQ + l * S * D, *dK = J->dK + l * S * D, *dV = J->dV + l * S * D;
+    for (int64_t x = 0; x < S * D; ++x) dQ[x] = dK[x] = dV[x] = 0.0;
+    for (int64_t q = 0; q < S; ++q) {
+        const uint16_t *qrow = J->Q + (l * S + q) * D;
+        const uint16_t *dorow = J->dO + (l * S + q) * D;
+        int64_t i = q / block, n = 0;
+        for (int32_t e = J->row_ptr[i]; e < J->row_ptr[i + 1]; ++e) {
+            int64_t j = J->col_idx[e];
+            for (int64_t k = j * block; k < (j + 1) * block; ++k)
+                if (k <= q) keys[n++] = k;
+        }
+        if (n == 0) continue;
+        double m = -INFINITY;
+        for (int64_t a = 0; a < n; ++a) {
+            const uint16_t *krow = J->K + (l * S + keys[a]) * D;
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d) dot += tab[qrow[d]] * tab[krow[d]];
+            p[a] = J->scale * dot;
+            if (p[a] > m) m = p[a];
+        }
+        double den = 0.0;
+        for (int64_t a = 0; a < n; ++a) {
+            p[a] = exp(p[a] - m);
+            den += p[a];
+        }
+        for (int64_t a = 0; a < n; ++a) p[a] /= den;
+        for (int64_t d = 0; d < D; ++d) o[d] = 0.0;
+        for (int64_t a = 0; a < n; ++a) {
+            const uint16_t *vrow = J->V + (l * S + keys[a]) * D;
+            for (int64_t d = 0; d < D; ++d) o[d] += p[a] * tab[vrow[d]];
+        }
+        double delta = 0.0;
+        for (int64_t d = 0; d < D; ++d) delta += tab[dorow[d]] * o[d];
+        for (int64_t a = 0; a < n; ++a) {
+            const int64_t k = keys[a];
+            const uint16_t *krow = J->K + (l * S + k) * D;
+            const uint16_t *vrow = J->V + (l * S + k) * D;
+            double dp = 0.0;
+            for (int64_t d = 0; d < D; ++d) dp += tab[dorow[d]] * tab[vrow[d]];
+            const double ds = p[a] * (dp - delta);
+            for (int64_t d = 0; d < D; ++d) {
+                dQ[q * D + d] += J->scale * ds * tab[krow[d]];
+                dK[k * D + d] += J->scale * ds * tab[qrow[d]];
+                dV[k * D + d] += p[a] * tab[dorow[d]];
+            }
+        }
+    }
+}
+
+static void *backward_worker(void *arg)
+{
+    bwd_job_t *J = (bwd_job_t *)arg;
+    double *p = (double *)malloc(sizeof(double) * (size_t)J->S);
+    int64_t *keys = (int64_t *)malloc(sizeof(int64_t) * (size_t)J->S);
+    double *o = (double *)malloc(sizeof(double) * (size_t)J->D);
+    if (p && keys && o)
+        for (int64_t l = J->lane_begin; l < J->lane_end; ++l) backward_lane(J, l, p, keys, o);
+    free(p);
+    free(keys);
+    free(o);
+    return NULL;
+}
+
+/* dQ, dK, dV are [L][S][D] binary64 outputs; dO is [L][S][D] 16-bit like Q. */
+int oracle_attention_backward(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                              const uint16_t *dO, int dtype, int64_t L, int64_t S, int64_t D,
+                              int64_t block, double scale, const int32_t *row_ptr,
+                              const int32_t *col_idx, double *dQ, double *dK, double *dV,
+                              int nthreads)
+{
+    if (block <= 0 || S % block != 0 || L <= 0 || D <= 0) return 1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (nthreads > L) nthreads = (int)L;
+    bwd_job_t base;
+    base.Q = Q; base.K = K; base.V = V; base.dO = dO;
+    base.tab = decode_table(dtype);
+    base.S = S; base.D = D; base.block = block; base.scale = scale;
+    base.row_ptr = row_ptr; base.col_idx = col_idx;
+    base.dQ = dQ; base.dK = dK; base.dV = dV;
+    bwd_job_t jobs[256];
+    pthread_t th[256];
+    int started[256];
+    int64_t chunk = (L + nthreads - 1) / nthreads;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t] = base;
+        jobs[t].lane_begin = t * chunk < L ? t * chunk : L;
+        jobs[t].lane_end = (t + 1) * chunk < L ? (t + 1) * chunk : L;
+        started[t] = 0;
+        if (t > 0 && jobs[t].lane_begin < jobs[t].lane_end)
+            started[t] = pthread_create(&th[t], NULL, backward_worker, &jobs[t]) == 0;
+    }
+    backward_worker(&jobs[0]);
+    for (int t = 1; t < nthreads; ++t) {
+        if (started[t]) pthread_join(th[t], NULL);
+        else if (jobs[t].lane_begin < jobs[t].lane_end) backward_worker(&jobs[t]);
     }
     return 0;
 }
