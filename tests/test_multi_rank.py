@@ -39,4 +39,6 @@ def test_two_ranks_take_max_time_and_sum_work():
 def test_single_rank_is_identity():
     import bench
     assert bench.aggregate_over_ranks(5.0, 2.0, torch.device("cpu"), 1) == (5.0, 2.0)
-    assert bench.launches_per_step(True) == 5 and bench.launches_per_step(False) == 1
+    assert bench.launches_per_step("topology") == 5 and bench.launches_per_step("dense") == 1
+    assert bench.launches_per_step("topology-content") == 7
+    assert bench.launches_per_step("segment:512") == 3 and bench.launches_per_step("density:0.1") == 1
