@@ -14,7 +14,9 @@
  *                              (block index, or centroid content).
  *   tsa_scheduled_attention -- forward causal attention that visits, for each 64-token query
  *                              block, only the key blocks in its CSR row (online softmax,
- *                              token-level causal mask in the diagonal block).
+ *                              token-level causal mask in the diagonal block);
+ *                              tsa_scheduled_attention_fwd also writes the row log-sum-exp.
+ *   tsa_scheduled_attention_backward -- dQ, dK, dV of that attention over the same CSR.
  *
  * Conventions shared by every call:
  *   - Every pointer argument except `salience_sq` is required.  Buffers are DEVICE memory
@@ -203,6 +205,54 @@ tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
                                    const int32_t *row_ptr, const int32_t *col_idx, void *O,
                                    tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
                                    int64_t block, float scale, tsa_stream_t stream);
+
+/*
+ * tsa_scheduled_attention that also writes, for every query row, the log-sum-exp of its scaled
+ * scores over the allowed keys: lse[l][q] = log(sum_{k allowed} exp(scale * <Q[l][q], K[l][k]>))
+ * (natural log; -inf for a row without keys).  The backward pass recomputes P from it.
+ *
+ *   lse  out, [B*H, S] float32 device array, 4-byte aligned (16-byte for the backward call),
+ *        or NULL (then this is tsa_scheduled_attention).
+ * Arguments, limits and errors otherwise as tsa_scheduled_attention.
+ */
+tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void *V,
+                                       const int32_t *row_ptr, const int32_t *col_idx, void *O,
+                                       float *lse, tsa_dtype dtype, int64_t B, int64_t H, int64_t S,
+                                       int64_t D, int64_t block, float scale, tsa_stream_t stream);
+
+/*
+ * Backward pass of the scheduled attention (the mirror page's segment-boundary record notes
+ * that the merged kernel has none; this is the chain rule of the forward above).  With P the
+ * softmax of the scaled scores over each query's allowed keys and dO the upstream gradient:
+ *   Delta_q = <dO_q, O_q>,  dS = P o (dO V^T - Delta),
+ *   dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q
+ * per lane, fp32 accumulation from the 16-bit inputs, results rounded to the input dtype.  P is
+ * recomputed from `lse` as written by tsa_scheduled_attention_fwd for the same inputs and CSR.
+ *
+ *   Q, K, V, O, dO  in,  [B*H, S, D] of `dtype`, 16-byte aligned; O is the forward's output.
+ *   lse             in,  [B*H, S] float32 from tsa_scheduled_attention_fwd, 16-byte aligned.
+ *   row_ptr, col_idx the CSR the forward ran with; nnz_cap >= its nnz (row_ptr[nb]), e.g. the
+ *                   length of col_idx.
+ *   dQ, dK, dV      out, [B*H, S, D] of `dtype`, 16-byte aligned, overlapping no input and no
+ *                   other output.
+ *   workspace       >= tsa_attention_backward_workspace_bytes(B*H, S, block, nnz_cap) bytes,
+ *                   256-byte aligned (Delta per row, the transposed schedule and its bitmap of
+ *                   nb^2 bits); its contents on entry do not matter.
+ *
+ * Limits: block == 64, D in {64, 128}, S % 64 == 0, nb = S/64 <= 8192, B*H <= 65535,
+ * B*H*S < 2^31.  Errors: INVALID_ARGUMENT, UNSUPPORTED, CAPACITY (workspace), NOT_DEVICE_POINTER,
+ * DEVICE_MISMATCH, CUDA.  Device-side: BAD_SCHEDULE (a row is cut at its first bad entry, as in
+ * the forward), TSA_ERR_DEVICE (nnz above nnz_cap: dK and dV then come out zero), TIMEOUT.
+ */
+size_t tsa_attention_backward_workspace_bytes(int64_t lanes, int64_t S, int64_t block,
+                                              int64_t nnz_cap);
+tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const void *V,
+                                            const void *O, const void *dO, const float *lse,
+                                            const int32_t *row_ptr, const int32_t *col_idx,
+                                            int64_t nnz_cap, void *dQ, void *dK, void *dV,
+                                            tsa_dtype dtype, int64_t B, int64_t H, int64_t S,
+                                            int64_t D, int64_t block, float scale, void *workspace,
+                                            size_t workspace_bytes, tsa_stream_t stream);
 
 /* Size of the device array behind tsa_build_schedule_noalloc: 16 MiB on every device that
  * loads the library, held until the process exits. */

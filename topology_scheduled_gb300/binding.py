@@ -49,6 +49,12 @@ SIGNATURES = {
     "tsa_scheduled_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
                                                _I64, _I64, _I64, ctypes.c_float, _P]),
     "tsa_last_device_status": (ctypes.c_int, [_P]),
+    "tsa_scheduled_attention_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
+                                                   _I64, _I64, _I64, ctypes.c_float, _P]),
+    "tsa_attention_backward_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
+    "tsa_scheduled_attention_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P,
+                                                        ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
+                                                        ctypes.c_float, _P, _SZ, _P]),
 }
 
 
@@ -212,17 +218,36 @@ def tsa_dense_causal_csr(S: int, block: int = 64, device=None, stream=None):
     return row_ptr, col_idx[:nnz] if nnz > 0 else col_idx[:0]
 
 
+def _check_qkv(**tensors):
+    ref = None
+    for name, t in tensors.items():
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+        if ref is not None and (t.shape != ref.shape or t.dtype != ref.dtype):
+            raise ValueError(f"{', '.join(tensors)} must share shape and dtype")
+        ref = t
+
+
+def _check_csr(row_ptr, col_idx):
+    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
+        raise TypeError("row_ptr and col_idx must be int32 (the CSR schedule dtype)")
+
+
 def tsa_scheduled_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
                             row_ptr: torch.Tensor, col_idx: torch.Tensor, scale: float | None = None,
                             *, out: torch.Tensor | None = None, block: int = 64, stream=None):
     """CSR-scheduled causal attention forward; output in the input dtype and shape."""
-    for name, t in (("Q", Q), ("K", K), ("V", V)):
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    if not (Q.shape == K.shape == V.shape) or not (Q.dtype == K.dtype == V.dtype):
-        raise ValueError("Q, K, V must share shape and dtype")
-    if row_ptr.dtype != torch.int32 or col_idx.dtype != torch.int32:
-        raise TypeError("row_ptr and col_idx must be int32 (the CSR schedule dtype)")
+    return tsa_scheduled_attention_fwd(Q, K, V, row_ptr, col_idx, scale, out=out, block=block,
+                                       stream=stream, with_lse=False)
+
+
+def tsa_scheduled_attention_fwd(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
+                                row_ptr: torch.Tensor, col_idx: torch.Tensor, scale: float | None = None,
+                                *, out: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                                block: int = 64, stream=None, with_lse: bool = True):
+    """Forward that also returns the per-row log-sum-exp ([B*H, S] float32) for the backward."""
+    _check_qkv(Q=Q, K=K, V=V)
+    _check_csr(row_ptr, col_idx)
     B, H, S, D = _lanes_S_D(Q)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -230,12 +255,48 @@ def tsa_scheduled_attention(Q: torch.Tensor, K: torch.Tensor, V: torch.Tensor,
         out = torch.empty_like(Q)
     elif out.shape != Q.shape or out.dtype != Q.dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous tensor with Q's shape and dtype")
+    if with_lse and lse is None:
+        lse = torch.empty((B * H, S), dtype=torch.float32, device=Q.device)
     ci = col_idx if col_idx.numel() > 0 else torch.zeros(1, dtype=torch.int32, device=Q.device)
-    _check(lib().tsa_scheduled_attention(Q.data_ptr(), K.data_ptr(), V.data_ptr(),
-                                         row_ptr.data_ptr(), ci.data_ptr(), out.data_ptr(),
-                                         _dtype_code(Q), B, H, S, D, block, float(scale),
-                                         _stream(stream)), "tsa_scheduled_attention")
-    return out
+    _check(lib().tsa_scheduled_attention_fwd(Q.data_ptr(), K.data_ptr(), V.data_ptr(),
+                                             row_ptr.data_ptr(), ci.data_ptr(), out.data_ptr(),
+                                             lse.data_ptr() if with_lse else None,
+                                             _dtype_code(Q), B, H, S, D, block, float(scale),
+                                             _stream(stream)), "tsa_scheduled_attention_fwd")
+    return (out, lse) if with_lse else out
+
+
+def tsa_attention_backward_workspace_bytes(lanes: int, S: int, block: int, nnz_cap: int) -> int:
+    return int(lib().tsa_attention_backward_workspace_bytes(lanes, S, block, nnz_cap))
+
+
+def tsa_scheduled_attention_backward(Q, K, V, O, dO, lse, row_ptr, col_idx, scale: float | None = None,
+                                     *, block: int = 64, dq=None, dk=None, dv=None, workspace=None,
+                                     stream=None):
+    """dQ, dK, dV of the scheduled attention for upstream gradient dO (input dtype and shape)."""
+    _check_qkv(Q=Q, K=K, V=V, O=O, dO=dO)
+    _check_csr(row_ptr, col_idx)
+    B, H, S, D = _lanes_S_D(Q)
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or lse.numel() != B * H * S:
+        raise ValueError("lse must be a contiguous float32 tensor of B*H*S elements")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ci = col_idx if col_idx.numel() > 0 else torch.zeros(1, dtype=torch.int32, device=Q.device)
+    nnz_cap = ci.numel()
+    ws = tsa_attention_backward_workspace_bytes(B * H, S, block, nnz_cap)
+    if ws == 0:
+        raise TsaError(2, "tsa_attention_backward_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(ws, dtype=torch.uint8, device=Q.device)
+    dq = torch.empty_like(Q) if dq is None else dq
+    dk = torch.empty_like(K) if dk is None else dk
+    dv = torch.empty_like(V) if dv is None else dv
+    _check(lib().tsa_scheduled_attention_backward(
+        Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), dO.data_ptr(), lse.data_ptr(),
+        row_ptr.data_ptr(), ci.data_ptr(), nnz_cap, dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+        _dtype_code(Q), B, H, S, D, block, float(scale), workspace.data_ptr(), workspace.numel(),
+        _stream(stream)), "tsa_scheduled_attention_backward")
+    return dq, dk, dv
 
 
 def tsa_last_device_status(stream=None) -> int:

@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtsa.so")
 
-SOURCES = ["api.cu", "schedule.cu", "segment.cu", "attention.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "schedule.cu", "segment.cu", "attention.cu", "backward.cu", "noalloc.cu"]
 HEADERS = [os.path.join(CSRC, "tsa_device.cuh"), os.path.join(CSRC, "tsa_internal.h"),
            os.path.join(INCLUDE, "tsa.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -24,7 +24,14 @@ std::mutex g_mutex;
 std::atomic<unsigned> g_epoch{0};
 
 tsa_status current_device(int *dev) {
-    if (cudaGetDevice(dev) != cudaSuccess) {
+    // Launch errors are read back with cudaGetLastError after each launch; an error an earlier
+    // call on this thread left pending (another library's, e.g. on an autograd worker thread)
+    // is cleared first so that it is not reported as this call's.
+    (void)cudaGetLastError();
+    // cudaSetDevice binds the device's primary context to this thread: a thread that has not
+    // touched the runtime yet (a worker thread) has no current context, and encoding a tensor
+    // map needs one.
+    if (cudaGetDevice(dev) != cudaSuccess || cudaSetDevice(*dev) != cudaSuccess) {
         cudaGetLastError();
         return TSA_ERR_CUDA;
     }
@@ -277,6 +284,14 @@ tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
                                    const int32_t *row_ptr, const int32_t *col_idx, void *O,
                                    tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
                                    int64_t block, float scale, tsa_stream_t stream) {
+    return tsa_scheduled_attention_fwd(Q, K, V, row_ptr, col_idx, O, nullptr, dtype, B, H, S, D, block,
+                                       scale, stream);
+}
+
+tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void *V,
+                                       const int32_t *row_ptr, const int32_t *col_idx, void *O,
+                                       float *lse, tsa_dtype dtype, int64_t B, int64_t H, int64_t S,
+                                       int64_t D, int64_t block, float scale, tsa_stream_t stream) {
     if (!Q || !K || !V || !row_ptr || !col_idx || !O) return TSA_ERR_INVALID_ARGUMENT;
     if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
@@ -288,14 +303,22 @@ tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
     if (lanes * S >= (int64_t)INT_MAX) return TSA_ERR_UNSUPPORTED;
     for (const void *p : {Q, K, V, static_cast<const void *>(O)})
         if (reinterpret_cast<uintptr_t>(p) & 15u) return TSA_ERR_INVALID_ARGUMENT;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return TSA_ERR_INVALID_ARGUMENT;
     const size_t bytes = (size_t)(lanes * S * D) * 2;
     if (overlaps(O, bytes, Q, bytes) || overlaps(O, bytes, K, bytes) || overlaps(O, bytes, V, bytes))
         return TSA_ERR_INVALID_ARGUMENT;
+    if (lse) {
+        const size_t lb = (size_t)(lanes * S) * 4;
+        if (overlaps(lse, lb, Q, bytes) || overlaps(lse, lb, K, bytes) || overlaps(lse, lb, V, bytes) ||
+            overlaps(lse, lb, O, bytes))
+            return TSA_ERR_INVALID_ARGUMENT;
+    }
     int dev;
     TSA_TRY(current_device(&dev));
     for (const void *p : {Q, K, V, static_cast<const void *>(O), static_cast<const void *>(row_ptr),
                           static_cast<const void *>(col_idx)})
         TSA_TRY(check_device_ptr(p, dev));
+    if (lse) TSA_TRY(check_device_ptr(lse, dev));
     const bool bf16 = dtype == TSA_BF16;
     const uint64_t rows = (uint64_t)(lanes * S);
     CUtensorMap tmQ, tmK, tmV, tmO;
@@ -309,6 +332,7 @@ tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
     a.tmO = &tmO;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;
+    a.lse = lse;
     a.nb = (int)(S / block);
     a.S = (int)S;
     a.D = (int)D;
@@ -318,6 +342,101 @@ tsa_status tsa_scheduled_attention(const void *Q, const void *K, const void *V,
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     TSA_TRY(device_flags(dev, &a.flags));
     return launch_scheduled_attention(a);
+}
+
+size_t tsa_attention_backward_workspace_bytes(int64_t lanes, int64_t S, int64_t block, int64_t nnz_cap) {
+    if (lanes <= 0 || S <= 0 || block != 64 || S % block != 0 || nnz_cap < 1) return 0;
+    const int64_t nb = S / block;
+    if (nb > kMaxBackwardBlocks || lanes * S >= (int64_t)INT_MAX) return 0;
+    return backward_workspace_layout(lanes, S, nb, nnz_cap).total;
+}
+
+tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const void *V, const void *O,
+                                            const void *dO, const float *lse, const int32_t *row_ptr,
+                                            const int32_t *col_idx, int64_t nnz_cap, void *dQ, void *dK,
+                                            void *dV, tsa_dtype dtype, int64_t B, int64_t H, int64_t S,
+                                            int64_t D, int64_t block, float scale, void *workspace,
+                                            size_t workspace_bytes, tsa_stream_t stream) {
+    if (!Q || !K || !V || !O || !dO || !lse || !row_ptr || !col_idx || !dQ || !dK || !dV || !workspace)
+        return TSA_ERR_INVALID_ARGUMENT;
+    if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
+    if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0 || nnz_cap < 1) return TSA_ERR_INVALID_ARGUMENT;
+    if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
+    if (block != 64 || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
+    if (S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
+    const int64_t lanes = B * H, nb = S / block;
+    if (lanes * S >= (int64_t)INT_MAX || nb > kMaxBackwardBlocks) return TSA_ERR_UNSUPPORTED;
+    const void *ins[] = {Q, K, V, O, dO};
+    void *outs[] = {dQ, dK, dV};
+    for (const void *p : ins)
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return TSA_ERR_INVALID_ARGUMENT;
+    for (const void *p : outs)
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return TSA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(lse) & 15u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return TSA_ERR_INVALID_ARGUMENT;
+    const size_t bytes = (size_t)(lanes * S * D) * 2;
+    for (int x = 0; x < 3; ++x) {
+        for (const void *p : ins)
+            if (overlaps(outs[x], bytes, p, bytes)) return TSA_ERR_INVALID_ARGUMENT;
+        if (overlaps(outs[x], bytes, lse, (size_t)(lanes * S) * 4)) return TSA_ERR_INVALID_ARGUMENT;
+        for (int y = x + 1; y < 3; ++y)
+            if (overlaps(outs[x], bytes, outs[y], bytes)) return TSA_ERR_INVALID_ARGUMENT;
+    }
+    const BwdWorkspace ws = backward_workspace_layout(lanes, S, nb, nnz_cap);
+    if (workspace_bytes < ws.total) return TSA_ERR_CAPACITY;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    for (const void *p : ins) TSA_TRY(check_device_ptr(p, dev));
+    for (const void *p : outs) TSA_TRY(check_device_ptr(p, dev));
+    for (const void *p : {static_cast<const void *>(lse), static_cast<const void *>(row_ptr),
+                          static_cast<const void *>(col_idx), static_cast<const void *>(workspace)})
+        TSA_TRY(check_device_ptr(p, dev));
+    const bool bf16 = dtype == TSA_BF16;
+    const uint64_t rows = (uint64_t)(lanes * S), cols = (uint64_t)D;
+    CUtensorMap tQ128, tdO128, tK128, tV128, tQ64, tdO64, tK64, tV64, tdQ64, tdK64, tdV64;
+    if (!encode_2d(&tQ128, Q, bf16, rows, cols, 128) || !encode_2d(&tdO128, dO, bf16, rows, cols, 128) ||
+        !encode_2d(&tK128, K, bf16, rows, cols, 128) || !encode_2d(&tV128, V, bf16, rows, cols, 128) ||
+        !encode_2d(&tQ64, Q, bf16, rows, cols, 64) || !encode_2d(&tdO64, dO, bf16, rows, cols, 64) ||
+        !encode_2d(&tK64, K, bf16, rows, cols, 64) || !encode_2d(&tV64, V, bf16, rows, cols, 64) ||
+        !encode_2d(&tdQ64, dQ, bf16, rows, cols, 64) || !encode_2d(&tdK64, dK, bf16, rows, cols, 64) ||
+        !encode_2d(&tdV64, dV, bf16, rows, cols, 64))
+        return TSA_ERR_CUDA;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    BwdLaunch a;
+    a.tmQ128 = &tQ128;
+    a.tmdO128 = &tdO128;
+    a.tmK128 = &tK128;
+    a.tmV128 = &tV128;
+    a.tmQ64 = &tQ64;
+    a.tmdO64 = &tdO64;
+    a.tmK64 = &tK64;
+    a.tmV64 = &tV64;
+    a.tmdQ64 = &tdQ64;
+    a.tmdK64 = &tdK64;
+    a.tmdV64 = &tdV64;
+    a.O = static_cast<const uint16_t *>(O);
+    a.dO = static_cast<const uint16_t *>(dO);
+    a.lse = lse;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.nnz_cap = nnz_cap;
+    a.delta = reinterpret_cast<float *>(w + ws.delta);
+    a.vlen = reinterpret_cast<int *>(w + ws.vlen);
+    a.cnt = reinterpret_cast<int *>(w + ws.cnt);
+    a.col_ptr = reinterpret_cast<int *>(w + ws.col_ptr);
+    a.bitmap = reinterpret_cast<unsigned *>(w + ws.bitmap);
+    a.bitmap_bytes = ws.bitmap_bytes;
+    a.row_idx = reinterpret_cast<int32_t *>(w + ws.row_idx);
+    a.nb = (int)nb;
+    a.S = (int)S;
+    a.D = (int)D;
+    a.lanes = (int)lanes;
+    a.bf16 = bf16;
+    a.scale = scale;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    TSA_TRY(device_flags(dev, &a.flags));
+    return launch_attention_backward(a);
 }
 
 tsa_status tsa_last_device_status(tsa_stream_t stream) {

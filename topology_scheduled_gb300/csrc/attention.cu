@@ -26,7 +26,8 @@
 //    than 2^8; the final O / l uses the same stale maximum, so the result is unchanged.  The
 //    decision is per row but TMEM loads/stores are warp-collective, so a warp rescales when
 //    any of its rows must (factor 1 for the others).
-//  * Epilogue.  O / l rounded to the input dtype, staged in the Q tile, TMA-stored per block.
+//  * Epilogue.  O / l rounded to the input dtype, staged in the Q tile, TMA-stored per block;
+//    optionally the row's log-sum-exp (m + log l), which the backward pass recomputes P from.
 //  * Two CTAs share an SM, so one CTA's softmax also overlaps the other's MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA records TSA_ERR_TIMEOUT, drains its
 // in-flight copies and MMAs (bounded), frees TMEM and returns.
@@ -146,7 +147,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmV,
                            const __grid_constant__ CUtensorMap tmO,
                            const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
-                           int nb, int S, float scale_log2, DeviceFlags flags) {
+                           float *__restrict__ lse_out, int nb, int S, float scale_log2, DeviceFlags flags) {
     using L = AttnSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -451,6 +452,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (*abort_flag == 0) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            // log-sum-exp of the scaled scores in natural-log units, for the backward pass
+            if (lse_out && row_exists)
+                lse_out[row0 + qa * kBlock + tid] =
+                    l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
             const uint32_t sw = (uint32_t)(tid & 7);
             __syncwarp();
 #pragma unroll
@@ -519,7 +524,8 @@ tsa_status launch_one(const AttnLaunch &a) {
     const int npairs = (a.nb + 1) / 2;
     dim3 grid((unsigned)npairs, (unsigned)a.lanes);
     kern<<<grid, kThreads, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
-                                                            a.col_idx, a.nb, a.S, a.scale_log2, a.flags);
+                                                            a.col_idx, a.lse, a.nb, a.S, a.scale_log2,
+                                                            a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }
 

@@ -22,6 +22,7 @@ __host__ __device__ constexpr int kAttnSmemBytes() {
 struct AttnLaunch {
     const CUtensorMap *tmQ, *tmK, *tmV, *tmO;
     const int32_t *row_ptr, *col_idx;
+    float *lse;  // optional: natural-log log-sum-exp of the scaled scores per query row
     int nb, S, D, lanes;
     bool bf16;
     float scale_log2;
@@ -30,6 +31,37 @@ struct AttnLaunch {
 };
 
 tsa_status launch_scheduled_attention(const AttnLaunch &a);
+
+// Byte offsets of the backward pass's workspace regions (each 256-byte aligned).
+struct BwdWorkspace {
+    size_t delta, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, total;
+};
+BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap);
+
+// Largest number of query blocks the backward pass accepts (its column bitmap is nb^2 bits).
+constexpr int64_t kMaxBackwardBlocks = 8192;
+
+struct BwdLaunch {
+    // 128-row boxes (tiles resident in a CTA) and 64-row boxes (streamed blocks, stores)
+    const CUtensorMap *tmQ128, *tmdO128, *tmK128, *tmV128;
+    const CUtensorMap *tmQ64, *tmdO64, *tmK64, *tmV64, *tmdQ64, *tmdK64, *tmdV64;
+    const uint16_t *O, *dO;
+    const float *lse;
+    const int32_t *row_ptr, *col_idx;
+    int64_t nnz_cap;
+    float *delta;
+    int *vlen, *cnt, *col_ptr;
+    unsigned *bitmap;
+    size_t bitmap_bytes;
+    int32_t *row_idx;
+    int nb, S, D, lanes;
+    bool bf16;
+    float scale;
+    DeviceFlags flags;
+    cudaStream_t stream;
+};
+
+tsa_status launch_attention_backward(const BwdLaunch &a);
 
 // Largest number of blocks the schedule builder accepts.
 constexpr int64_t kMaxScheduleBlocks = 4096;
