@@ -15,6 +15,12 @@ Schedules built on the GPU inside every step: "topology" (elder rule, index ties
 "topology-content" (content ties), "segment:TOKENS" (fixed segments).  "dense" and
 "density:P" are built once before timing.
 
+--pass bwd times the backward instead: one step = tsa_scheduled_attention_backward (the
+transposed schedule, Delta = rowsum(dO * O), the dQ kernel and the dK/dV kernel) over a schedule
+built once before timing, with O and the log-sum-exp from one forward call.  Its FLOPs count the
+five 64 x 64 x D block products of the gradient on visited blocks (S recomputation excluded):
+nnz * lanes * 10 * 64^2 * D per step.
+
 --impl reference times the CPU oracle (oracle/, fp64) on the host cores on a bounded
 sample of the same workload.
 """
@@ -55,6 +61,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--heads", type=int, default=0,
                    help="override H (a smaller case of the same workload, e.g. for ncu captures)")
+    p.add_argument("--pass", dest="pass_", choices=["fwd", "bwd"], default="fwd",
+                   help="time the forward step (default) or the backward call")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="target CPU time of the oracle's attention sample")
     return p.parse_args()
@@ -279,6 +287,8 @@ def run_gpu(args):
         raise RuntimeError(f"device status {tsa.STATUS_NAMES.get(status, status)}")
     nnz = int(row_ptr[-1].item())
     flops = visited_flops(nnz, w.lanes, w.D, w.block)
+    if args.pass_ == "bwd":
+        return run_backward(args, w, tsa, q, k, v, row_ptr, col_idx, nnz, dev, world, rank, local)
     n_launch = launches_per_step(args.schedule)
     for _ in range(max(args.warmup, 0)):
         step()
@@ -376,6 +386,117 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+BWD_LAUNCHES = 7  # bwd_rows, bwd_col_count, bwd_col_scan, bwd_col_fill, bwd_delta, bwd_dq, bwd_dkv
+
+
+def run_backward(args, w, tsa, q, k, v, row_ptr, col_idx, nnz, dev, world, rank, local):
+    """--pass bwd: time tsa_scheduled_attention_backward alone (schedule built once before)."""
+    import torch.distributed as dist
+
+    stream = torch.cuda.current_stream()
+    O, lse = tsa.tsa_scheduled_attention_fwd(q, k, v, row_ptr, col_idx, w.scale)
+    g = torch.Generator(device=dev).manual_seed(1000 + rank)
+    dO = torch.randn(q.shape, generator=g, device=dev, dtype=torch.float32).to(q.dtype)
+    ws = torch.empty(tsa.tsa_attention_backward_workspace_bytes(w.lanes, w.S, w.block, col_idx.numel()),
+                     dtype=torch.uint8, device=dev)
+    dq, dk, dv = (torch.empty_like(q) for _ in range(3))
+
+    def step():
+        tsa.tsa_scheduled_attention_backward(q, k, v, O, dO, lse, row_ptr, col_idx, w.scale,
+                                             dq=dq, dk=dk, dv=dv, workspace=ws)
+
+    step()
+    status = tsa.tsa_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {tsa.STATUS_NAMES.get(status, status)}")
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = ev(), ev()
+    host0 = time.time()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop(host0, host1)
+    status = tsa.tsa_last_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status after timing {tsa.STATUS_NAMES.get(status, status)}")
+    flops = 2.5 * visited_flops(nnz, w.lanes, w.D, w.block)
+    elapsed_ms, flops_all = aggregate_over_ranks(t0.elapsed_time(t1), flops, dev, world)
+    ms = elapsed_ms / args.steps
+    value = flops_all * args.steps / (elapsed_ms * 1e-3) / 1e12
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "scheduled-attn bwd TFLOP/s on visited blocks (5 block products); ms/call",
+        "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_name(w.dtype),
+        "data": "synthetic (seeded N(0,1) Q/V/dO, clustered K; no dataset)",
+        "config": {
+            "workload": f"{w.name}: {w.describe()}", "schedule": args.schedule, "pass": "bwd",
+            "B": w.B, "H": w.H, "S": w.S, "D": w.D, "block": w.block, "nnz_blocks": nnz,
+            "visited_flops_per_step": flops,
+            "l2": "inputs larger than L2 (Q,K,V,O,dO %.2f GB per rank), no flush"
+                  % (5 * q.numel() * q.element_size() / 1e9),
+            "parallelism": f"independent problem per rank x{world} (no collective)",
+        },
+        "roofline": {
+            "kernel": "tsa_scheduled_attention_backward (all launches of the call)",
+            "bound": "tensor", "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": f"{peak_kind} bf16_tflops_sustained (cuBLAS bf16, seconds-long loop)",
+            "traffic": None,
+        },
+        "gpu_launches": BWD_LAUNCHES * args.steps,
+        "clocks": clk,
+        "e2e": None,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_backward(args, w, q, k, v, dO, row_ptr, col_idx, nnz)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline_backward(args, w, q, k, v, dO, row_ptr, col_idx, nnz):
+    """The fp64 CPU oracle's backward on whole lanes, one at a time until the time budget."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    S, D = w.S, w.D
+    rp = row_ptr.cpu().numpy()
+    ci = col_idx.cpu().numpy()[: rp[-1]]
+    sl = lambda t, i: t.reshape(-1, S, D)[i:i + 1].cpu()  # noqa: E731
+    done, spent = 0, 0.0
+    while done < w.lanes and spent < args.cpu_seconds:
+        a = [sl(t, done) for t in (q, k, v, dO)]
+        t0 = time.perf_counter()
+        oracle.attention_backward(*a, rp, ci, w.block, w.scale, nthreads=threads)
+        spent += time.perf_counter() - t0
+        done += 1
+    step_s = spent * w.lanes / done
+    flops_all = 2.5 * visited_flops(nnz, w.lanes, D, w.block)
+    return {"value": round(flops_all / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"backward of {done} of {w.lanes} lanes ({spent:.1f} s), extrapolated by lanes; "
+                      f"step estimate {step_s:.1f} s"}
 
 
 def run_e2e(args, w, tsa, q, k, v, out, build, row_ptr, col_idx, topo, flops, stream, world):
