@@ -407,31 +407,25 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 // p = 2^(x * scale * log2(e) - m): one packed FMA per pair, exp2 on the MUFU
                 const uint64_t cc = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm = f2_pack(-m_used, -m_used);
-                uint64_t acc0 = f2_pack(0.f, 0.f), acc1 = acc0;
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
                     float e0, e1;
                     f2_unpack(f2_fma(f2_pack(x[2 * t], x[2 * t + 1]), cc, nm), e0, e1);
                     const float p0 = ex2_approx(e0), p1 = ex2_approx(e1);
-                    // The denominator sums the rounded P that the PV product uses, so a row
-                    // dominated by one key normalizes exactly.
-                    uint64_t rounded;
                     if constexpr (kBF16) {
                         const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
                         pw[t] = *reinterpret_cast<const uint32_t *>(&h);
-                        rounded = f2_pack(__uint_as_float(pw[t] << 16), __uint_as_float(pw[t] & 0xFFFF0000u));
                     } else {
                         const __half2 h = __floats2half2_rn(p0, p1);
                         pw[t] = *reinterpret_cast<const uint32_t *>(&h);
-                        rounded = f2_pack(__low2float(h), __high2float(h));
                     }
-                    if (t & 1) acc1 = f2_add(acc1, rounded);
-                    else acc0 = f2_add(acc0, rounded);
+                    // The denominator sums the rounded P that the PV product uses, so a row
+                    // dominated by one key normalizes exactly.
+                    add_half<kBF16, false>(ls[(t & 1) * 2], pw[t]);
+                    add_half<kBF16, true>(ls[(t & 1) * 2 + 1], pw[t]);
                 }
-                float a0, a1, b0, b1;
-                f2_unpack(acc0, a0, a1);
-                f2_unpack(acc1, b0, b1);
-                l_sum += (a0 + b0) + (a1 + b1);
+                l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             } else {
 #pragma unroll
                 for (int t = 0; t < 32; ++t) pw[t] = 0u;

@@ -333,6 +333,17 @@ __device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
     return d;
 }
 
+// acc += the 16-bit float (f16 or bf16) in the low or high half of w, widened exactly: one
+// mixed-precision add (f32 = 16-bit + f32), so no unpacking instructions are needed.
+template <bool kBF16, bool kHigh>
+__device__ __forceinline__ void add_half(float &acc, uint32_t w) {
+    const unsigned short h = kHigh ? (unsigned short)(w >> 16) : (unsigned short)(w & 0xFFFFu);
+    if constexpr (kBF16)
+        asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(acc) : "h"(h));
+    else
+        asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(acc) : "h"(h));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
