@@ -9,8 +9,9 @@
 //  * Tile.  One CTA computes 128 query rows: query blocks 2p and 2p+1 of one lane, because
 //    tcgen05 runs at full rate at M = 128.  It walks the sorted union of the two CSR rows; a
 //    key block in only one row is masked for the other half (each half is two whole warps).
-//  * Warp roles (192 threads).  Warp 4 produces: TMA loads of Q once and of the K/V tiles of
-//    each visited block into a two-stage ring (128-byte swizzle).  Warp 5 issues the MMAs from
+//  * Warp roles (192 threads).  Warp 4 produces: one thread TMA-loads Q once and the K and V
+//    tiles of each visited block into two-stage rings of their own (128-byte swizzle), polling
+//    both rings so that neither stream waits behind the other.  Warp 5 issues the MMAs from
 //    one thread: S = Q K^T (M128 N64 K=D, both operands in shared memory) into one of two TMEM
 //    S buffers, and O += P V (M128 N=D K64) with P read from TMEM.  Warps 0-3 run the online
 //    softmax, one row per thread: tcgen05.ld of the S row, exp2 with the scale folded in, the
@@ -41,7 +42,8 @@ namespace {
 
 constexpr int kRows = 128;            // query rows per CTA (two 64-token query blocks)
 constexpr int kBlock = 64;            // tokens per key / query block
-constexpr int kStages = 2;            // K/V ring depth
+constexpr int kKStages = 2;           // K ring depth
+constexpr int kVStages = 2;           // V ring depth
 constexpr int kThreads = 192;         // 4 softmax warps + producer warp + MMA warp
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -53,9 +55,9 @@ struct AttnSmem {
     static constexpr int kQBytes = kRows * D * 2;     // Q tile, later the O staging tile
     static constexpr int kKVBytes = kBlock * D * 2;   // one K or V tile
     static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;                // kStages tiles
-    static constexpr int kOffV = kOffK + kStages * kKVBytes;     // kStages tiles
-    static constexpr int kOffMeta = kOffV + kStages * kKVBytes;
+    static constexpr int kOffK = kOffQ + kQBytes;                // kKStages tiles
+    static constexpr int kOffV = kOffK + kKStages * kKVBytes;    // kVStages tiles
+    static constexpr int kOffMeta = kOffV + kVStages * kKVBytes;
     static constexpr int kMetaBytes = 256;
     static constexpr int kTmemCols = 256;  // S0 | S1 | O (P_b aliases the first 32 of S_b)
     static constexpr int kOCol = 128;
@@ -64,20 +66,24 @@ struct AttnSmem {
 __device__ __forceinline__ uint32_t s_col(int b) { return b ? 64u : 0u; }
 
 // Meta area layout (byte offsets from kOffMeta).
-constexpr int kMetaRing = 4;     // union entries in flight (K ring runs up to 2 ahead of softmax)
+// Union entries in flight: the producer writes entry v once QK(v - kKStages) is done, while the
+// softmax warps may still be about to read entry v - kKStages - 1, so the ring holds more.
+constexpr int kMetaRing = 8;
+static_assert(kMetaRing >= kKStages + 2, "meta ring shorter than the K ring's lead");
 constexpr int kBarQ = 0;
-constexpr int kBarKFull = 8;     // kStages x 8
-constexpr int kBarKEmpty = 24;   // kStages x 8
-constexpr int kBarVFull = 40;    // kStages x 8
-constexpr int kBarVEmpty = 56;   // kStages x 8
-constexpr int kBarSFull = 72;    // 2 x 8
-constexpr int kBarPFull = 88;    // 2 x 8
-constexpr int kBarODone = 104;
-constexpr int kBarFin = 112;
-constexpr int kTmemSlot = 120;
-constexpr int kAbortFlag = 124;
-constexpr int kMetaJ = 128;      // kMetaRing x 4
-constexpr int kMetaF = 144;      // kMetaRing x 4
+constexpr int kBarKFull = 8;                          // kKStages x 8
+constexpr int kBarKEmpty = kBarKFull + 8 * kKStages;  // kKStages x 8
+constexpr int kBarVFull = kBarKEmpty + 8 * kKStages;  // kVStages x 8
+constexpr int kBarVEmpty = kBarVFull + 8 * kVStages;  // kVStages x 8
+constexpr int kBarSFull = kBarVEmpty + 8 * kVStages;  // 2 x 8
+constexpr int kBarPFull = kBarSFull + 16;             // 2 x 8
+constexpr int kBarODone = kBarPFull + 16;
+constexpr int kBarFin = kBarODone + 8;
+constexpr int kTmemSlot = kBarFin + 8;
+constexpr int kAbortFlag = kTmemSlot + 4;
+constexpr int kMetaJ = kAbortFlag + 4;                // kMetaRing x 4
+constexpr int kMetaF = kMetaJ + 4 * kMetaRing;        // kMetaRing x 4
+static_assert(kMetaF + 4 * kMetaRing <= 256, "meta area");
 
 // Walks the union of two sorted CSR rows (query blocks qa and qa+1), checking the row
 // contract on the way.  Used by the producer thread.
@@ -140,6 +146,11 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, float &sum) {
     }
 }
 
+// The layout leaves at least 512 bytes for aligning the dynamic shared-memory base to 1024
+// (the kernel checks the actual alignment and reports kDevSmemAlign if it does not fit).
+static_assert(AttnSmem<128>::kOffMeta + AttnSmem<128>::kMetaBytes + 512 <= kAttnSmemBytes<128>(), "smem");
+static_assert(AttnSmem<64>::kOffMeta + AttnSmem<64>::kMetaBytes + 512 <= kAttnSmemBytes<64>(), "smem");
+
 template <int D, bool kBF16>
 __global__ void __launch_bounds__(kThreads, 2)
 scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -190,9 +201,11 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
 
     if (tid == 0) {
         mbar_init(bar_q, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(BAR_K_FULL(s), 1);
             mbar_init(BAR_K_EMPTY(s), 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(BAR_V_FULL(s), 1);
             mbar_init(BAR_V_EMPTY(s), 1);
         }
@@ -217,55 +230,86 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer (TMA)
+        // One thread, two independent streams: the K tile of union entry v goes into K stage
+        // v % kKStages as soon as QK(v - kKStages) has freed it, the V tile into V stage
+        // v % kVStages as soon as PV(v - kVStages) has; the thread polls both rings, so a K
+        // load never waits behind a V stage.
         if ((tid & 31) == 0) {
             tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmO);
-            RowUnion ru;
-            ru.init(row_ptr, col_idx, qa, has_b);
+            RowUnion ruk, ruv;  // each stream walks the row union on its own
+            ruk.init(row_ptr, col_idx, qa, has_b);
+            ruv.init(row_ptr, col_idx, qa, has_b);
             mbar_arrive_expect_tx(bar_q, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
                 tma_load_2d(sQ + c * 16384, &tmQ, c * 64, row0 + qa * kBlock, bar_q);
-            // Entry v: K into stage v % kStages once QK(v - kStages) is done, V into its stage
-            // once PV(v - kStages) is done; K therefore runs ahead of V.
-            bool ok = true;
-            int v = 0, k_issued = 0, v_issued = 0;
-            for (;; ++v) {
-                const int s = v % kStages;
-                const uint32_t par = (uint32_t)((v / kStages) - 1) & 1u;
-                if (v >= kStages && !mbar_wait(BAR_K_EMPTY(s), par, flags)) { ok = false; break; }
-                int f = 0;
-                const int j = ru.next(f);
-                meta_j[v % kMetaRing] = j;
-                meta_f[v % kMetaRing] = f;
-                if (j < 0) {
-                    mbar_arrive(BAR_K_FULL(s));
-                    break;
+            bool ok = true, k_done = false, v_done = false;
+            int kv = 0, vv = 0;  // next union entry of each stream
+            unsigned long long t_idle = 0;
+            for (uint32_t it = 0; !(k_done && v_done); ++it) {
+                bool progress = false;
+                if (!k_done && (kv < kKStages ||
+                                mbar_try_wait(BAR_K_EMPTY(kv % kKStages), (uint32_t)((kv / kKStages) - 1) & 1u))) {
+                    const int s = kv % kKStages;
+                    int f = 0;
+                    const int j = ruk.next(f);
+                    meta_j[kv % kMetaRing] = j;
+                    meta_f[kv % kMetaRing] = f;
+                    if (j < 0) {
+                        mbar_arrive(BAR_K_FULL(s));  // the end marker travels with the K ring
+                        k_done = true;
+                    } else {
+                        mbar_arrive_expect_tx(BAR_K_FULL(s), L::kKVBytes);
+#pragma unroll
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_2d(sK0 + s * L::kKVBytes + c * 8192, &tmK, c * 64, row0 + j * kBlock,
+                                        BAR_K_FULL(s));
+                        ++kv;
+                    }
+                    progress = true;
                 }
-                const int y = row0 + j * kBlock;
-                mbar_arrive_expect_tx(BAR_K_FULL(s), L::kKVBytes);
+                if (!v_done && (vv < kVStages ||
+                                mbar_try_wait(BAR_V_EMPTY(vv % kVStages), (uint32_t)((vv / kVStages) - 1) & 1u))) {
+                    const int s = vv % kVStages;
+                    int f = 0;
+                    const int j = ruv.next(f);
+                    if (j < 0) {
+                        v_done = true;
+                    } else {
+                        mbar_arrive_expect_tx(BAR_V_FULL(s), L::kKVBytes);
 #pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_2d(sK0 + s * L::kKVBytes + c * 8192, &tmK, c * 64, y, BAR_K_FULL(s));
-                k_issued = v + 1;
-                if (v >= kStages && !mbar_wait(BAR_V_EMPTY(s), par, flags)) { ok = false; break; }
-                mbar_arrive_expect_tx(BAR_V_FULL(s), L::kKVBytes);
-#pragma unroll
-                for (int c = 0; c < L::kChunks; ++c)
-                    tma_load_2d(sV0 + s * L::kKVBytes + c * 8192, &tmV, c * 64, y, BAR_V_FULL(s));
-                v_issued = v + 1;
+                        for (int c = 0; c < L::kChunks; ++c)
+                            tma_load_2d(sV0 + s * L::kKVBytes + c * 8192, &tmV, c * 64, row0 + j * kBlock,
+                                        BAR_V_FULL(s));
+                        ++vv;
+                    }
+                    progress = true;
+                }
+                // bounded: give up after kWaitTimeoutNs without progress, or when the launch did
+                if (progress) {
+                    t_idle = 0;
+                } else if ((it & 63u) == 0u) {
+                    const unsigned long long now = globaltimer();
+                    if (t_idle == 0) t_idle = now;
+                    if (now - t_idle > kWaitTimeoutNs ||
+                        *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch) {
+                        ok = false;
+                        break;
+                    }
+                }
             }
-            if (ru.bad) raise_status(flags, kDevBadSchedule);
+            if (ruk.bad) raise_status(flags, kDevBadSchedule);
             if (!ok) {
                 // Drain: wait (bounded) for every load issued into the rings.
                 *abort_flag = 1;
                 (void)mbar_wait_timed(bar_q, 0);
-                for (int w = k_issued - kStages; w < k_issued; ++w)
-                    if (w >= 0) (void)mbar_wait_timed(BAR_K_FULL(w % kStages), (w / kStages) & 1);
-                for (int w = v_issued - kStages; w < v_issued; ++w)
-                    if (w >= 0) (void)mbar_wait_timed(BAR_V_FULL(w % kStages), (w / kStages) & 1);
+                for (int w = kv - kKStages; w < kv; ++w)
+                    if (w >= 0) (void)mbar_wait_timed(BAR_K_FULL(w % kKStages), (w / kKStages) & 1);
+                for (int w = vv - kVStages; w < vv; ++w)
+                    if (w >= 0) (void)mbar_wait_timed(BAR_V_FULL(w % kVStages), (w / kVStages) & 1);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -276,10 +320,10 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             bool ok = mbar_wait(bar_q, 0, flags);
             int u = 0;
             bool have = false;  // entry u exists and QK(u) was issued
-            // QK(u): S_{u%2} = Q K_u^T; frees K stage u % kStages when done
+            // QK(u): S_{u%2} = Q K_u^T; frees K stage u % kKStages when done
 #define ISSUE_QK(uu)                                                                              \
     do {                                                                                          \
-        const int s_ = (uu) % kStages;                                                            \
+        const int s_ = (uu) % kKStages;                                                           \
         tc_fence_after();                                                                         \
         _Pragma("unroll") for (int kk = 0; kk < D / 16; ++kk) {                                   \
             const uint64_t a_ = sdesc_sw128(sQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);    \
@@ -306,8 +350,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             while (ok && have) {
                 // next scores first, so they overlap the softmax of u
                 bool next = false;
-                const int s1 = (u + 1) % kStages;
-                ok = mbar_wait(BAR_K_FULL(s1), ((u + 1) / kStages) & 1, flags);
+                const int s1 = (u + 1) % kKStages;
+                ok = mbar_wait(BAR_K_FULL(s1), ((u + 1) / kKStages) & 1, flags);
                 if (!ok) break;
                 if (meta_j[(u + 1) % kMetaRing] >= 0) {
                     ISSUE_QK(u + 1);
@@ -318,8 +362,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 // O += P_u V_u once the softmax has written P_u and V_u has landed
                 ok = mbar_wait(BAR_P_FULL(u & 1), (u >> 1) & 1, flags);
                 if (!ok) break;
-                const int s = u % kStages;
-                ok = mbar_wait(BAR_V_FULL(s), (u / kStages) & 1, flags);
+                const int s = u % kVStages;
+                ok = mbar_wait(BAR_V_FULL(s), (u / kVStages) & 1, flags);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -362,8 +406,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             __syncwarp();
             if (in_row) {
                 uint32_t sr[2][32];
-                tmem_ld32(s_addr, sr[0]);
-                tmem_ld32(s_addr + 32, sr[1]);
+                tmem_ld32x2(s_addr, sr[0], sr[1]);
                 float x[64];  // raw scores q.k
 #pragma unroll
                 for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);

@@ -245,6 +245,37 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// Two TMEM loads of this warp's 32 lanes x 32 columns (columns taddr.. and taddr+32..) with a
+// single wait, so the two round trips overlap.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, uint32_t (&r)[32], uint32_t (&q)[32]) {
+#define TSA_LD32(dst, addr)                                                                            \
+    asm volatile(                                                                                      \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                                      \
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "                      \
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"      \
+        : "=r"(dst[0]), "=r"(dst[1]), "=r"(dst[2]), "=r"(dst[3]), "=r"(dst[4]), "=r"(dst[5]),          \
+          "=r"(dst[6]), "=r"(dst[7]), "=r"(dst[8]), "=r"(dst[9]), "=r"(dst[10]), "=r"(dst[11]),        \
+          "=r"(dst[12]), "=r"(dst[13]), "=r"(dst[14]), "=r"(dst[15]), "=r"(dst[16]), "=r"(dst[17]),    \
+          "=r"(dst[18]), "=r"(dst[19]), "=r"(dst[20]), "=r"(dst[21]), "=r"(dst[22]), "=r"(dst[23]),    \
+          "=r"(dst[24]), "=r"(dst[25]), "=r"(dst[26]), "=r"(dst[27]), "=r"(dst[28]), "=r"(dst[29]),    \
+          "=r"(dst[30]), "=r"(dst[31])                                                                 \
+        : "r"(addr)                                                                                    \
+        : "memory")
+#define TSA_HOLD32(dst)                                                                                \
+    "+r"(dst[0]), "+r"(dst[1]), "+r"(dst[2]), "+r"(dst[3]), "+r"(dst[4]), "+r"(dst[5]), "+r"(dst[6]), \
+        "+r"(dst[7]), "+r"(dst[8]), "+r"(dst[9]), "+r"(dst[10]), "+r"(dst[11]), "+r"(dst[12]),         \
+        "+r"(dst[13]), "+r"(dst[14]), "+r"(dst[15]), "+r"(dst[16]), "+r"(dst[17]), "+r"(dst[18]),      \
+        "+r"(dst[19]), "+r"(dst[20]), "+r"(dst[21]), "+r"(dst[22]), "+r"(dst[23]), "+r"(dst[24]),      \
+        "+r"(dst[25]), "+r"(dst[26]), "+r"(dst[27]), "+r"(dst[28]), "+r"(dst[29]), "+r"(dst[30]),      \
+        "+r"(dst[31])
+    TSA_LD32(r, taddr);
+    TSA_LD32(q, taddr + 32);
+    // the wait names both destinations so that no use or copy of them moves above it
+    asm volatile("tcgen05.wait::ld.sync.aligned;" : TSA_HOLD32(r), TSA_HOLD32(q) : : "memory");
+#undef TSA_LD32
+#undef TSA_HOLD32
+}
+
 // TMEM load of this warp's 32 lanes x 16 columns into 16 registers (wait fused, as above).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
     asm volatile(
