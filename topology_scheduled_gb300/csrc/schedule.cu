@@ -385,9 +385,9 @@ __global__ void __launch_bounds__(64) pairwise_d2(const double *__restrict__ C, 
 //     key (d2, min(u,v), max(u,v))); CTA 0 takes each component's lightest edge, hooks along
 //     it (a mutual pair keeps the smaller label as root), records each chosen edge once,
 //     flattens by pointer jumping and relabels.  The rounds stop at one component.
-//   Elder rule (CTA 0): bitonic sort of the nb-1 MST edges by the same key, then one warp
-//     merges in that order: the smaller component is absorbed (size tie: the root with the
-//     larger index) and its root receives the edge's d2.
+//   Elder rule (CTA 0): bitonic sort of the nb-1 MST edges by the same key, then one thread
+//     merges in that order with a union-find in shared memory: the smaller component is
+//     absorbed (size tie: the root with the larger index) and its root receives the edge's d2.
 //   CSR: every CTA sorts the blocks by (salience desc, index asc); warps count each row's
 //     blocks from a per-row bitmap (sink range, local window, first topk blocks <= i of the
 //     order); CTA 0 scans the counts into row_ptr; warps fill col_idx in ascending order.
@@ -620,30 +620,13 @@ __device__ void bitonic_sort_regs(unsigned long long &k1, unsigned long long &k2
     }
 }
 
-// 16-way select of v[s] (s in [0, 16)) as a depth-4 tree of selects (no local memory).
-__device__ __forceinline__ int select16(const int (&v)[16], int s) {
-    int t[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) t[k] = (s & 1) ? v[2 * k + 1] : v[2 * k];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) t[k] = (s & 2) ? t[2 * k + 1] : t[2 * k];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) t[k] = (s & 4) ? t[2 * k + 1] : t[2 * k];
-    return (s & 8) ? t[1] : t[0];
-}
-
-// Lane l of the merging warp keeps the root labels of blocks l, l+32, ... in registers (up
-// to 32 * kLabelRegs blocks; beyond that the labels live in shared memory).  A root label is
-// read with a branch-free select of the slot and a shuffle from the owning lane.
-constexpr int kLabelRegs = 16;
-
 // CTA 0: elder-rule salience from the MST edges.
 __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsigned long long *xs) {
     const int nb = a.nb, pow2 = a.pow2;
     unsigned long long *kd = reinterpret_cast<unsigned long long *>(sm);
     unsigned long long *kab = kd + pow2;
     volatile int *size = reinterpret_cast<volatile int *>(kab + pow2);
-    volatile int *label = size + nb;  // used only when nb > 32 * kLabelRegs
+    volatile int *label = size + nb;  // union-find parents
     const int ne = nb - 1;
     // under content ties the merges run on ranks: salience goes to a rank-indexed scratch and
     // is scattered to blocks at the end (one global write per merge, no dependent load)
@@ -664,7 +647,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
         sal[v] = 0.0;
     }
     __syncthreads();
-    const bool fast = nb <= 32 * kLabelRegs && pow2 <= (int)blockDim.x;
+    const bool fast = pow2 <= (int)blockDim.x;
     if (fast) {
         // one element per thread (padding sorts last), sorted copy written back to kd/kab
         unsigned long long k1 = threadIdx.x < pow2 ? kd[threadIdx.x] : ~0ull;
@@ -680,67 +663,46 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     } else {
         bitonic_sort_pairs(kd, kab, pow2);
     }
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        if (fast) {
-            // Everything in registers: lane l holds the root label and, for roots, the
-            // component size of blocks l + 32k; edges arrive 32 at a time and are broadcast.
-            int lab[kLabelRegs], sz[kLabelRegs];
-#pragma unroll
-            for (int k = 0; k < kLabelRegs; ++k) {
-                lab[k] = lane + 32 * k;
-                sz[k] = 1;
+    // Merges in edge order, one thread, union-find in shared memory.  The smaller component is
+    // absorbed (on a size tie the root with the larger index), so linking the absorbed root
+    // under the survivor is union by size: trees stay O(log nb) deep, path halving keeps them
+    // flatter, and the root of a component is always its survivor -- the one block of it that
+    // has received no merge distance yet.
+    if (threadIdx.x == 0) {
+        int *par = const_cast<int *>(label);
+        int *siz = const_cast<int *>(size);
+        for (int e = 0; e < ne; ++e) {
+            const unsigned long long ab = kab[e];
+            const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
+            if (x < 0 || x >= nb || y < 0 || y >= nb) {
+                raise_status(a.flags, kDevCapacity);
+                break;
             }
-            for (int e0 = 0; e0 < ne; e0 += 32) {
-                const unsigned long long my_ab = e0 + lane < ne ? kab[e0 + lane] : 0ull;
-                const unsigned long long my_d = e0 + lane < ne ? kd[e0 + lane] : 0ull;
-                const int cnt = min(32, ne - e0);
-                for (int j = 0; j < cnt; ++j) {
-                    const unsigned long long ab = __shfl_sync(0xffffffffu, my_ab, j);
-                    const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
-                    const int rx = __shfl_sync(0xffffffffu, select16(lab, (x >> 5) & 15), x & 31);
-                    const int ry = __shfl_sync(0xffffffffu, select16(lab, (y >> 5) & 15), y & 31);
-                    const int sx = __shfl_sync(0xffffffffu, select16(sz, (rx >> 5) & 15), rx & 31);
-                    const int sy = __shfl_sync(0xffffffffu, select16(sz, (ry >> 5) & 15), ry & 31);
-                    int absorbed, survivor;
-                    if (sx < sy) { absorbed = rx; survivor = ry; }
-                    else if (sy < sx) { absorbed = ry; survivor = rx; }
-                    else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
-                    const bool merge = rx != ry;  // always true for MST edges
-                    const bool owner = lane == (survivor & 31);
-#pragma unroll
-                    for (int k = 0; k < kLabelRegs; ++k) {
-                        lab[k] = (merge && lab[k] == absorbed) ? survivor : lab[k];
-                        sz[k] = (merge && owner && k == (survivor >> 5)) ? sx + sy : sz[k];
-                    }
-                    if (merge && lane == j)
-                        sal[absorbed] = __longlong_as_double((long long)my_d);
+            int rx = x, ry = y;
+            // both finds at once (independent loads overlap); at most nb steps each
+            for (int it = 0; it < nb; ++it) {
+                const int px = par[rx], py = par[ry];
+                if (px == rx && py == ry) break;
+                if (px != rx) {
+                    const int gx = par[px];
+                    par[rx] = gx;
+                    rx = gx;
+                }
+                if (py != ry) {
+                    const int gy = par[py];
+                    par[ry] = gy;
+                    ry = gy;
                 }
             }
-        } else {
-            for (int e = 0; e < ne; ++e) {
-                const unsigned long long ab = kab[e];
-                const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
-                if (x < 0 || x >= nb || y < 0 || y >= nb) {
-                    if (lane == 0) raise_status(a.flags, kDevCapacity);
-                    break;
-                }
-                const int rx = label[x], ry = label[y];
-                if (rx == ry) continue;  // cannot happen for MST edges
-                const int sx = size[rx], sy = size[ry];
-                int absorbed, survivor;
-                if (sx < sy) { absorbed = rx; survivor = ry; }
-                else if (sy < sx) { absorbed = ry; survivor = rx; }
-                else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
-                __syncwarp();
-                for (int v = lane; v < nb; v += 32)
-                    if (label[v] == absorbed) label[v] = survivor;
-                if (lane == 0) {
-                    size[survivor] = sx + sy;
-                    sal[absorbed] = __longlong_as_double((long long)kd[e]);
-                }
-                __syncwarp();
-            }
+            if (rx == ry) continue;  // cannot happen for MST edges
+            const int sx = siz[rx], sy = siz[ry];
+            int absorbed, survivor;
+            if (sx < sy) { absorbed = rx; survivor = ry; }
+            else if (sy < sx) { absorbed = ry; survivor = rx; }
+            else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
+            par[absorbed] = survivor;
+            siz[survivor] = sx + sy;
+            sal[absorbed] = __longlong_as_double((long long)kd[e]);
         }
     }
     __syncthreads();
