@@ -394,9 +394,8 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
         TSA_TRY(check_device_ptr(p, dev));
     const bool bf16 = dtype == TSA_BF16;
     const uint64_t rows = (uint64_t)(lanes * S), cols = (uint64_t)D;
-    CUtensorMap tQ128, tdO128, tK128, tV128, tQ64, tdO64, tK64, tV64, tdQ64, tdK64, tdV64;
+    CUtensorMap tQ128, tdO128, tQ64, tdO64, tK64, tV64, tdQ64, tdK64, tdV64;
     if (!encode_2d(&tQ128, Q, bf16, rows, cols, 128) || !encode_2d(&tdO128, dO, bf16, rows, cols, 128) ||
-        !encode_2d(&tK128, K, bf16, rows, cols, 128) || !encode_2d(&tV128, V, bf16, rows, cols, 128) ||
         !encode_2d(&tQ64, Q, bf16, rows, cols, 64) || !encode_2d(&tdO64, dO, bf16, rows, cols, 64) ||
         !encode_2d(&tK64, K, bf16, rows, cols, 64) || !encode_2d(&tV64, V, bf16, rows, cols, 64) ||
         !encode_2d(&tdQ64, dQ, bf16, rows, cols, 64) || !encode_2d(&tdK64, dK, bf16, rows, cols, 64) ||
@@ -406,8 +405,6 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     BwdLaunch a;
     a.tmQ128 = &tQ128;
     a.tmdO128 = &tdO128;
-    a.tmK128 = &tK128;
-    a.tmV128 = &tV128;
     a.tmQ64 = &tQ64;
     a.tmdO64 = &tdO64;
     a.tmK64 = &tK64;
@@ -428,6 +425,7 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     a.bitmap = reinterpret_cast<unsigned *>(w + ws.bitmap);
     a.bitmap_bytes = ws.bitmap_bytes;
     a.row_idx = reinterpret_cast<int32_t *>(w + ws.row_idx);
+    a.pairs = reinterpret_cast<int *>(w + ws.pairs);
     a.nb = (int)nb;
     a.S = (int)S;
     a.D = (int)D;

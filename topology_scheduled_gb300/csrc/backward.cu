@@ -165,6 +165,38 @@ __global__ void bwd_col_fill(int nb, int words, const unsigned *__restrict__ bit
     }
 }
 
+// One CTA: the key blocks sorted by the length of their transposed column (descending, then
+// by index) and paired in that order -- pairs[2p], pairs[2p+1] (-1 if nb is odd and p is the
+// last pair).  A dK/dV CTA walks the union of its two columns, so pairing a long column (a
+// sink or top-k block that nearly every query block holds) with a short one would leave half
+// of its 128-row tile idle for the whole long walk; sorted pairs also put the longest walks
+// first in launch order.  Bitonic sort of (~count << 32 | j) keys in shared memory.
+__global__ void __launch_bounds__(1024) bwd_col_pairs(int nb, int pow2, const int *__restrict__ cnt,
+                                                       int *__restrict__ pairs) {
+    extern __shared__ unsigned long long keys[];
+    for (int i = threadIdx.x; i < pow2; i += blockDim.x)
+        keys[i] = i < nb ? ((unsigned long long)(0xFFFFFFFFu - (unsigned)cnt[i]) << 32) | (unsigned)i : ~0ull;
+    __syncthreads();
+    for (int k = 2; k <= pow2; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
+                const int p = i ^ j;
+                if (p > i) {
+                    const unsigned long long a = keys[i], b = keys[p];
+                    if ((a > b) == ((i & k) == 0)) {
+                        keys[i] = b;
+                        keys[p] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    const int npairs = (nb + 1) >> 1;
+    for (int q = threadIdx.x; q < 2 * npairs; q += blockDim.x)
+        pairs[q] = q < nb ? (int)(keys[q] & 0xFFFFFFFFull) : -1;
+}
+
 // ---------------------------------------------------------------- Delta = rowsum(dO * O)
 template <bool kBF16>
 __device__ __forceinline__ float to_f32(uint32_t h16) {
@@ -615,8 +647,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
                const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                const int *__restrict__ col_ptr, const int32_t *__restrict__ row_idx,
-               const float *__restrict__ lse, const float *__restrict__ delta, int nb, int S,
-               float scale, float scale_log2, DeviceFlags flags) {
+               const int *__restrict__ pairs, const float *__restrict__ lse,
+               const float *__restrict__ delta, int nb, int S, float scale, float scale_log2,
+               DeviceFlags flags) {
     using L = DkvSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (__syncthreads_or(threadIdx.x == 0 &&
@@ -645,8 +678,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 
     const int tid = threadIdx.x, warp = tid >> 5;
     const int lane_id = blockIdx.x;
-    const int kp = 2 * (int)blockIdx.y;  // key blocks kp and kp+1; the longest columns come first
-    const bool has_b = kp + 1 < nb;
+    // key blocks ka and kb (-1: none) from the pair list, heaviest transposed columns first
+    const int ka = __ldg(pairs + 2 * blockIdx.y), kb = __ldg(pairs + 2 * blockIdx.y + 1);
+    const bool has_b = kb >= 0;
     const int row0 = lane_id * S;
 
     if (tid == 0) {
@@ -684,17 +718,20 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             tma_prefetch_desc(&tmdK);
             tma_prefetch_desc(&tmdV);
             ListUnion lu;
-            lu.a = row_idx + col_ptr[kp];
+            lu.a = row_idx + col_ptr[ka];
             lu.ia = 0;
-            lu.ia_end = col_ptr[kp + 1] - col_ptr[kp];
-            lu.b = has_b ? row_idx + col_ptr[kp + 1] : row_idx;
+            lu.ia_end = col_ptr[ka + 1] - col_ptr[ka];
+            lu.b = has_b ? row_idx + col_ptr[kb] : row_idx;
             lu.ib = 0;
-            lu.ib_end = has_b ? col_ptr[kp + 2] - col_ptr[kp + 1] : 0;
+            lu.ib_end = has_b ? col_ptr[kb + 1] - col_ptr[kb] : 0;
             mbar_arrive_expect_tx(bar_tile, 2 * L::kTileBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
-                tma_load_2d(sK + c * 16384, &tmK, c * 64, row0 + kp * kBlock, bar_tile);
-                tma_load_2d(sV + c * 16384, &tmV, c * 64, row0 + kp * kBlock, bar_tile);
+                tma_load_2d(sK + c * 16384, &tmK, c * 64, row0 + ka * kBlock, bar_tile);
+                tma_load_2d(sV + c * 16384, &tmV, c * 64, row0 + ka * kBlock, bar_tile);
+                // the second block's rows, or the first block's again (masked) if there is none
+                tma_load_2d(sK + c * 16384 + 8192, &tmK, c * 64, row0 + (has_b ? kb : ka) * kBlock, bar_tile);
+                tma_load_2d(sV + c * 16384 + 8192, &tmV, c * 64, row0 + (has_b ? kb : ka) * kBlock, bar_tile);
             }
             bool ok = true;
             int issued = 0;
@@ -803,9 +840,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         }
     } else {
         // ------------------------------------------------------------ elementwise (warps 0-3)
-        const int half = tid >> 6;               // key block kp + half
+        const int half = tid >> 6;               // 0: key block ka, 1: key block kb
         const int k_in = tid & 63;               // key token within its block
-        const int key_block = kp + half;
+        const int key_block = half ? kb : ka;
         const bool row_exists = half == 0 || has_b;
         const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
         bool ok = true;
@@ -873,11 +910,11 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             if (tid == 0) {
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_store_2d(&tmdV, c * 64, row0 + kp * kBlock, sV + c * 16384);
-                    tma_store_2d(&tmdK, c * 64, row0 + kp * kBlock, sK + c * 16384);
+                    tma_store_2d(&tmdV, c * 64, row0 + ka * kBlock, sV + c * 16384);
+                    tma_store_2d(&tmdK, c * 64, row0 + ka * kBlock, sK + c * 16384);
                     if (has_b) {
-                        tma_store_2d(&tmdV, c * 64, row0 + (kp + 1) * kBlock, sV + c * 16384 + 8192);
-                        tma_store_2d(&tmdK, c * 64, row0 + (kp + 1) * kBlock, sK + c * 16384 + 8192);
+                        tma_store_2d(&tmdV, c * 64, row0 + kb * kBlock, sV + c * 16384 + 8192);
+                        tma_store_2d(&tmdK, c * 64, row0 + kb * kBlock, sK + c * 16384 + 8192);
                     }
                 }
                 tma_store_commit();
@@ -914,8 +951,8 @@ tsa_status launch_grad_kernels(const BwdLaunch &a) {
     kq<<<grid, kThreads, DqSmem<D>::kBytes, a.stream>>>(*a.tmQ128, *a.tmdO128, *a.tmK64, *a.tmV64, *a.tmdQ64,
                                                         a.row_ptr, a.col_idx, a.vlen, a.lse, a.delta, a.nb,
                                                         a.S, a.scale, scale_log2, a.flags);
-    kkv<<<grid, kThreads, DkvSmem<D>::kBytes, a.stream>>>(*a.tmK128, *a.tmV128, *a.tmQ64, *a.tmdO64, *a.tmdK64,
-                                                          *a.tmdV64, a.col_ptr, a.row_idx, a.lse, a.delta,
+    kkv<<<grid, kThreads, DkvSmem<D>::kBytes, a.stream>>>(*a.tmK64, *a.tmV64, *a.tmQ64, *a.tmdO64, *a.tmdK64,
+                                                          *a.tmdV64, a.col_ptr, a.row_idx, a.pairs, a.lse, a.delta,
                                                           a.nb, a.S, a.scale, scale_log2, a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }
@@ -938,6 +975,7 @@ BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int
     w.bitmap = take(sizeof(unsigned) * (size_t)(nb * words));
     w.bitmap_bytes = sizeof(unsigned) * (size_t)(nb * words);
     w.row_idx = take(sizeof(int32_t) * (size_t)(nnz_cap > 0 ? nnz_cap : 1));
+    w.pairs = take(sizeof(int) * (size_t)(2 * ((nb + 1) / 2)));
     w.total = o;
     return w;
 }
@@ -952,6 +990,14 @@ tsa_status launch_attention_backward(const BwdLaunch &a) {
     bwd_col_count<<<wgrid, 256, 0, st>>>(nb, words, a.bitmap, a.cnt);
     bwd_col_scan<<<1, 1024, 0, st>>>(nb, a.cnt, a.col_ptr, (long long)a.nnz_cap, a.flags);
     bwd_col_fill<<<wgrid, 256, 0, st>>>(nb, words, a.bitmap, a.col_ptr, a.row_idx);
+    {
+        int pow2 = 1;
+        while (pow2 < nb) pow2 <<= 1;
+        const size_t smem = sizeof(unsigned long long) * (size_t)pow2;  // <= 64 KB (nb <= 8192)
+        if (cudaFuncSetAttribute(bwd_col_pairs, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+            return TSA_ERR_CUDA;
+        bwd_col_pairs<<<1, 1024, smem, st>>>(nb, pow2, a.cnt, a.pairs);
+    }
     {
         const long long items = (long long)a.lanes * a.S * (a.D / 8);
         const long long blocks = (items + 255) / 256;

@@ -34,7 +34,7 @@ tsa_status launch_scheduled_attention(const AttnLaunch &a);
 
 // Byte offsets of the backward pass's workspace regions (each 256-byte aligned).
 struct BwdWorkspace {
-    size_t delta, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, total;
+    size_t delta, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, pairs, total;
 };
 BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap);
 
@@ -43,7 +43,7 @@ constexpr int64_t kMaxBackwardBlocks = 8192;
 
 struct BwdLaunch {
     // 128-row boxes (tiles resident in a CTA) and 64-row boxes (streamed blocks, stores)
-    const CUtensorMap *tmQ128, *tmdO128, *tmK128, *tmV128;
+    const CUtensorMap *tmQ128, *tmdO128;
     const CUtensorMap *tmQ64, *tmdO64, *tmK64, *tmV64, *tmdQ64, *tmdK64, *tmdV64;
     const uint16_t *O, *dO;
     const float *lse;
@@ -54,6 +54,7 @@ struct BwdLaunch {
     unsigned *bitmap;
     size_t bitmap_bytes;
     int32_t *row_idx;
+    int *pairs;  // dK/dV key-block pairs, 2 per pair (-1: none)
     int nb, S, D, lanes;
     bool bf16;
     float scale;
