@@ -52,7 +52,7 @@ ATTN_SOURCE = os.path.join(ROOT, "topology_scheduled_gb300", "csrc", "attention.
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--steps", type=int, default=1000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["tsa", "reference"], default="tsa")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
