@@ -12,6 +12,8 @@
  *   tsa_segment_csr         -- the CSR of a segment mask (fixed or listed segment starts).
  *   tsa_build_schedule_ex   -- tsa_build_schedule with the elder rule's tie rule chosen
  *                              (block index, or centroid content).
+ *   tsa_block_sums / tsa_build_schedule_from_sums -- the same build in two halves, for keys
+ *                              whose lanes are spread over several GPUs.
  *   tsa_scheduled_attention -- forward causal attention that visits, for each 64-token query
  *                              block, only the key blocks in its CSR row (online softmax,
  *                              token-level causal mask in the diagonal block);
@@ -135,6 +137,37 @@ tsa_status tsa_build_schedule_ex(const void *K, tsa_dtype dtype, int64_t lanes, 
                                  int64_t topk, tsa_tie_break tie_break, int32_t *row_ptr,
                                  int32_t *col_idx, int64_t col_cap, double *salience_sq,
                                  void *workspace, size_t workspace_bytes, tsa_stream_t stream);
+
+/*
+ * The schedule build in two halves, for keys whose lanes are spread over several GPUs
+ * (the schedule is one CSR shared by all lanes, built from the lane-mean centroids).
+ *
+ * tsa_block_sums: per-lane block sums of this GPU's lanes, the first stage of
+ * tsa_build_schedule -- part[l][b][d] = sum over the block's tokens t (ascending) of
+ * K[l][b*block + t][d], in binary64, the same value tsa_build_schedule forms internally.
+ *   K     [lanes, S, D] f16/bf16, device (this GPU's lanes, contiguous).
+ *   part  device buffer of lanes * (S / block) * D doubles, written.
+ * Limits and errors as tsa_build_schedule.
+ *
+ * tsa_build_schedule_from_sums: the rest of tsa_build_schedule_ex from the block sums of ALL
+ * lanes: centroid C[b][d] = (sum over l ascending of part[l][b][d]) / (block * lanes), then
+ * distances, MST, elder rule, top-k and CSR exactly as there.  Gather every GPU's block sums
+ * in global lane order (an all-gather of lanes * nb * D doubles) and call this on each GPU:
+ * every GPU gets the CSR, bit for bit, that tsa_build_schedule_ex returns for all the keys
+ * on one GPU.  (Summing per-GPU totals instead would re-associate the lane sum.)
+ *   part        [lanes][nb][D] binary64, device, read only.
+ *   S           nb * block (the sequence length the CSR is for).
+ *   workspace   >= tsa_build_schedule_workspace_bytes(lanes, S, D, block) bytes.
+ * Other arguments, limits and errors as tsa_build_schedule_ex.
+ */
+tsa_status tsa_block_sums(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S, int64_t D,
+                          int64_t block, double *part, tsa_stream_t stream);
+tsa_status tsa_build_schedule_from_sums(const double *part, int64_t lanes, int64_t S, int64_t D,
+                                        int64_t block, int64_t sink, int64_t local_radius,
+                                        int64_t topk, tsa_tie_break tie_break, int32_t *row_ptr,
+                                        int32_t *col_idx, int64_t col_cap, double *salience_sq,
+                                        void *workspace, size_t workspace_bytes,
+                                        tsa_stream_t stream);
 
 /*
  * Segment schedules ("Add topology-derived sparse attention kernel" mirror page, the later

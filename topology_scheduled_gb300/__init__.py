@@ -10,11 +10,14 @@ its operations with the same names:
 * ``tsa_fixed_segment_csr`` / ``tsa_segment_csr`` -- the CSR of a segment mask;
 * ``tsa_scheduled_attention`` -- causal attention over a CSR block schedule
   (``tsa_scheduled_attention_fwd`` also returns the row log-sum-exp);
-* ``tsa_scheduled_attention_backward`` -- its dQ, dK, dV.
+* ``tsa_scheduled_attention_backward`` -- its dQ, dK, dV;
+* ``tsa_block_sums`` / ``tsa_build_schedule_from_sums`` -- the build in two halves, for keys
+  whose lanes are spread over several GPUs (``distributed.build_schedule_lane_sharded``).
 """
 from .binding import (STATUS_NAMES, TIE_RULES, TSA_BF16, TSA_F16, TsaError, lib,  # noqa: F401
                       library_path, tsa_build_schedule, tsa_build_schedule_workspace_bytes,
                       tsa_dense_causal_csr, tsa_fixed_segment_csr, tsa_fixed_segment_nnz,
                       tsa_last_device_status, tsa_schedule_max_nnz, tsa_scheduled_attention,
                       tsa_scheduled_attention_fwd, tsa_scheduled_attention_backward,
-                      tsa_attention_backward_workspace_bytes, tsa_segment_csr)
+                      tsa_attention_backward_workspace_bytes, tsa_segment_csr, tsa_block_sums,
+                      tsa_build_schedule_from_sums)

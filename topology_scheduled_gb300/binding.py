@@ -42,6 +42,9 @@ SIGNATURES = {
                                              ctypes.c_int, _P, _P, _I64, _P, _P, _SZ, _P]),
     "tsa_build_schedule_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _I64, _I64,
                                                   _I64, _P, _P, _I64, _P, _P]),
+    "tsa_block_sums": (ctypes.c_int, [_P, ctypes.c_int, _I64, _I64, _I64, _I64, _P, _P]),
+    "tsa_build_schedule_from_sums": (ctypes.c_int, [_P, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+                                                    ctypes.c_int, _P, _P, _I64, _P, _P, _SZ, _P]),
     "tsa_fixed_segment_nnz": (_I64, [_I64, _I64, _I64]),
     "tsa_fixed_segment_csr": (ctypes.c_int, [_I64, _I64, _I64, _P, _P, _I64, _P]),
     "tsa_segment_csr": (ctypes.c_int, [_I64, _I64, _P, _I64, _P, _P, _I64, _P]),
@@ -164,6 +167,55 @@ def tsa_build_schedule(K: torch.Tensor, block: int = 64, sink: int = 1, local_ra
                                    sal.data_ptr() if sal is not None else None,
                                    workspace.data_ptr(), workspace.numel(), _stream(stream)),
            "tsa_build_schedule_ex")
+    return (row_ptr, col_idx, sal) if salience else (row_ptr, col_idx)
+
+
+def tsa_block_sums(K: torch.Tensor, block: int = 64, *, out: torch.Tensor | None = None, stream=None):
+    """Per-lane block sums of K ([S, D], [L, S, D] or [B, H, S, D]): float64 [lanes, S/block, D]."""
+    if not K.is_cuda or not K.is_contiguous():
+        raise ValueError("K must be a contiguous CUDA tensor")
+    B, H, S, D = _lanes_S_D(K)
+    lanes = B * H
+    nb = S // block if block > 0 else 0
+    if out is None:
+        out = torch.empty((lanes, nb, D), dtype=torch.float64, device=K.device)
+    elif out.dtype != torch.float64 or not out.is_contiguous() or out.numel() != lanes * nb * D:
+        raise ValueError("out must be a contiguous float64 tensor of lanes * S/block * D elements")
+    _check(lib().tsa_block_sums(K.data_ptr(), _dtype_code(K), lanes, S, D, block, out.data_ptr(),
+                                _stream(stream)), "tsa_block_sums")
+    return out
+
+
+def tsa_build_schedule_from_sums(sums: torch.Tensor, block: int = 64, sink: int = 1, local_radius: int = 1,
+                                 topk: int = 2, *, salience: bool = False, tie_break: str = "index",
+                                 workspace: torch.Tensor | None = None, stream=None):
+    """tsa_build_schedule from the block sums of all lanes ([lanes, nb, D] float64, lanes in
+    global order, e.g. gathered from the GPUs that hold them).  Same result as
+    tsa_build_schedule on the full keys, bit for bit."""
+    if not sums.is_cuda or not sums.is_contiguous() or sums.dtype != torch.float64 or sums.dim() != 3:
+        raise ValueError("sums must be a contiguous CUDA float64 tensor [lanes, nb, D]")
+    if tie_break not in TIE_RULES:
+        raise ValueError(f"tie_break must be one of {sorted(TIE_RULES)}")
+    lanes, nb, D = sums.shape
+    S = nb * block
+    L = lib()
+    cap = int(L.tsa_schedule_max_nnz(S, block, sink, local_radius, topk))
+    if cap < 0:
+        raise TsaError(1, "tsa_schedule_max_nnz")
+    ws_bytes = int(L.tsa_build_schedule_workspace_bytes(lanes, S, D, block))
+    if ws_bytes == 0:
+        raise TsaError(2, "tsa_build_schedule_workspace_bytes")
+    dev = sums.device
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+    col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    sal = torch.empty(nb, dtype=torch.float64, device=dev) if salience else None
+    _check(L.tsa_build_schedule_from_sums(sums.data_ptr(), lanes, S, D, block, sink, local_radius, topk,
+                                          TIE_RULES[tie_break], row_ptr.data_ptr(), col_idx.data_ptr(),
+                                          col_idx.numel(), sal.data_ptr() if sal is not None else None,
+                                          workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "tsa_build_schedule_from_sums")
     return (row_ptr, col_idx, sal) if salience else (row_ptr, col_idx)
 
 

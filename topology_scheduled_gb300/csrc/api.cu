@@ -224,6 +224,82 @@ tsa_status tsa_build_schedule_ex(const void *K, tsa_dtype dtype, int64_t lanes, 
     return launch_build_schedule(a);
 }
 
+tsa_status tsa_block_sums(const void *K, tsa_dtype dtype, int64_t lanes, int64_t S, int64_t D,
+                          int64_t block, double *part, tsa_stream_t stream) {
+    if (!K || !part) return TSA_ERR_INVALID_ARGUMENT;
+    if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(K) & 1u) || (reinterpret_cast<uintptr_t>(part) & 7u))
+        return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = S / block;
+    if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
+    if (lanes > INT64_MAX / S / D) return TSA_ERR_INVALID_ARGUMENT;
+    if (overlaps(part, (size_t)(lanes * nb * D) * 8, K, (size_t)(lanes * S * D) * 2)) return TSA_ERR_INVALID_ARGUMENT;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    TSA_TRY(check_device_ptr(K, dev));
+    TSA_TRY(check_device_ptr(part, dev));
+    ScheduleLaunch a{};
+    a.K = static_cast<const uint16_t *>(K);
+    a.bf16 = dtype == TSA_BF16;
+    a.lanes = lanes;
+    a.S = S;
+    a.D = D;
+    a.block = block;
+    a.nb = nb;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    TSA_TRY(device_flags(dev, &a.flags));
+    return launch_block_sums(a, part);
+}
+
+tsa_status tsa_build_schedule_from_sums(const double *part, int64_t lanes, int64_t S, int64_t D,
+                                        int64_t block, int64_t sink, int64_t local_radius,
+                                        int64_t topk, tsa_tie_break tie_break, int32_t *row_ptr,
+                                        int32_t *col_idx, int64_t col_cap, double *salience_sq,
+                                        void *workspace, size_t workspace_bytes,
+                                        tsa_stream_t stream) {
+    if (!part || !row_ptr || !col_idx || !workspace) return TSA_ERR_INVALID_ARGUMENT;
+    if (tie_break != TSA_TIE_INDEX && tie_break != TSA_TIE_CONTENT) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (sink < 0 || local_radius < 0 || topk < 0) return TSA_ERR_INVALID_ARGUMENT;
+    if ((reinterpret_cast<uintptr_t>(part) & 7u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = S / block;
+    if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
+    if (lanes > INT64_MAX / nb / D / 8) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t need = max_nnz_bound(nb, sink, local_radius, topk);
+    if (col_cap < need) return TSA_ERR_CAPACITY;
+    const ScheduleWorkspace ws = schedule_workspace_layout(lanes, nb, D);
+    if (workspace_bytes < ws.total) return TSA_ERR_CAPACITY;
+    if (overlaps(part, (size_t)(lanes * nb * D) * 8, workspace, ws.total)) return TSA_ERR_INVALID_ARGUMENT;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    TSA_TRY(check_device_ptr(part, dev));
+    TSA_TRY(check_device_ptr(row_ptr, dev));
+    TSA_TRY(check_device_ptr(col_idx, dev));
+    TSA_TRY(check_device_ptr(workspace, dev));
+    if (salience_sq) TSA_TRY(check_device_ptr(salience_sq, dev));
+    ScheduleLaunch a{};
+    a.K = nullptr;
+    a.lanes = lanes;
+    a.S = S;
+    a.D = D;
+    a.block = block;
+    a.nb = nb;
+    a.sink = sink < nb ? sink : nb;
+    a.local_radius = local_radius < nb ? local_radius : nb;
+    a.topk = topk < nb ? topk : nb;
+    a.content_ties = tie_break == TSA_TIE_CONTENT;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.col_cap = col_cap;
+    a.salience_sq = salience_sq;
+    a.workspace = static_cast<uint8_t *>(workspace);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    TSA_TRY(device_flags(dev, &a.flags));
+    return launch_schedule_from_sums(a, part);
+}
+
 tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int32_t *col_idx,
                                 int64_t col_cap, tsa_stream_t stream) {
     if (!row_ptr || !col_idx) return TSA_ERR_INVALID_ARGUMENT;

@@ -936,7 +936,38 @@ ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D
     return w;
 }
 
+// Per-lane block sums of K into part[lanes][nb][D].
+tsa_status launch_block_sums(const ScheduleLaunch &a, double *part) {
+    cudaStream_t st = a.stream;
+    const bool vec = (a.D % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.K) & 15u) == 0);
+    const int64_t items = vec ? a.lanes * a.nb * (a.D / 8) : a.lanes * a.nb * a.D;
+    const int threads = 256;
+    const int64_t blocks = (items + threads - 1) / threads;
+    const unsigned grid = (unsigned)(blocks < 152 * 64 ? blocks : 152 * 64);
+    int log2_block = 0;
+    while ((int64_t(1) << log2_block) < a.block) ++log2_block;
+    const int spread_limit = 45 - log2_block;
+    if (vec)
+        centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
+                                                        spread_limit, part);
+    else
+        centroid_partial_scalar<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
+                                                          spread_limit, part);
+    return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
+}
+
 tsa_status launch_build_schedule(const ScheduleLaunch &a) {
+    const ScheduleWorkspace ws = schedule_workspace_layout(a.lanes, a.nb, a.D);
+    double *part = reinterpret_cast<double *>(a.workspace + ws.part);
+    const tsa_status st = launch_block_sums(a, part);
+    return st != TSA_OK ? st : launch_schedule_from_sums(a, part);
+}
+
+// Everything after the block sums: lane-mean centroids (lanes in ascending order), the
+// content ranking if asked, distances, and the graph kernel.  `sums` is read only; the
+// content rule's permuted centroids go to the workspace's own block-sum area, which is `sums`
+// itself when called from launch_build_schedule (the sums are no longer needed by then).
+tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums) {
     const int nb = (int)a.nb;
     const ScheduleWorkspace ws = schedule_workspace_layout(a.lanes, a.nb, a.D);
     uint8_t *w = a.workspace;
@@ -954,24 +985,10 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
     cudaStream_t st = a.stream;
 
     // centroids
-    const bool vec = (a.D % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.K) & 15u) == 0);
-    const int64_t items = vec ? a.lanes * a.nb * (a.D / 8) : a.lanes * a.nb * a.D;
-    const int threads = 256;
-    const int64_t blocks = (items + threads - 1) / threads;
-    const unsigned grid = (unsigned)(blocks < 152 * 64 ? blocks : 152 * 64);
-    int log2_block = 0;
-    while ((int64_t(1) << log2_block) < a.block) ++log2_block;
-    const int spread_limit = 45 - log2_block;
-    if (vec)
-        centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
-                                                        spread_limit, part);
-    else
-        centroid_partial_scalar<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
-                                                          spread_limit, part);
     {
         const int64_t n = a.nb * a.D;
         const unsigned g = (unsigned)((n + 255) / 256);
-        centroid_final<<<g, 256, 0, st>>>(part, a.lanes, a.nb, a.D, (double)(a.block * a.lanes), cent);
+        centroid_final<<<g, 256, 0, st>>>(sums, a.lanes, a.nb, a.D, (double)(a.block * a.lanes), cent);
     }
     // content rule: rank the blocks, run the graph on the centroids in rank order
     int *perm = nullptr;
@@ -982,7 +999,7 @@ tsa_status launch_build_schedule(const ScheduleLaunch &a) {
         const int64_t n = a.nb * a.D;
         permute_rows<<<(unsigned)((n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16), 256, 0, st>>>(
             cent, perm, a.nb, a.D, part);
-        graph_cent = part;  // the per-lane sums are no longer needed
+        graph_cent = part;  // the workspace's block-sum area; centroid_final has read the sums
     }
     // distances
     {

@@ -89,6 +89,10 @@ struct ScheduleLaunch {
 };
 
 tsa_status launch_build_schedule(const ScheduleLaunch &a);
+// The two halves of launch_build_schedule, for a lane-sharded build: per-lane block sums of K
+// (part: lanes x nb x D doubles), and the schedule from block sums of all lanes.
+tsa_status launch_block_sums(const ScheduleLaunch &a, double *part);
+tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums);
 tsa_status launch_dense_causal_csr(int64_t nb, int32_t *row_ptr, int32_t *col_idx,
                                    cudaStream_t stream);
 // Segment schedule: fixed segments of seg_tokens (> 0), or the listed starts (seg_tokens 0).
