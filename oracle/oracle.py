@@ -116,13 +116,14 @@ def dense_causal_csr(nb: int):
 
 
 def centroids(K, block: int, dtype: int | None = None) -> np.ndarray:
-    """Lane-mean key-block centroids, K shaped [L, S, D] (or [S, D])."""
+    """Lane-mean key-block centroids, K shaped [L, S, D] (or [S, D]); ceil(S / block) blocks,
+    a partial last block averaging the tokens it holds."""
     bits, dt = _bits(K, dtype)
     if bits.ndim == 2:
         bits = bits[None]
     bits = bits.reshape(-1, bits.shape[-2], bits.shape[-1])
     L, S, D = bits.shape
-    C = np.empty((S // block, D), dtype=np.float64)
+    C = np.empty((-(-S // block), D), dtype=np.float64)
     _check(lib().oracle_centroids(_p(bits), ctypes.c_int(dt), _I64(L), _I64(S), _I64(D),
                                   _I64(block), _p(C)), "centroids")
     return C
@@ -181,7 +182,7 @@ def build_schedule(K, block: int, sink: int, local_radius: int, topk: int,
         bits = bits[None]
     bits = bits.reshape(-1, bits.shape[-2], bits.shape[-1])
     L, S, D = bits.shape
-    nb = S // block
+    nb = -(-S // block)  # a partial last block is a block too
     cap = max(max_nnz(nb, sink, local_radius, topk), 1)
     row_ptr = np.empty(nb + 1, dtype=np.int32)
     col_idx = np.empty(cap, dtype=np.int32)

@@ -128,26 +128,30 @@ int oracle_dense_causal_csr(int64_t nb, int32_t *row_ptr, int32_t *col_idx)
  * K is [L][S][D] (L = batch*heads lanes, one shared schedule).  Reading: the
  * point cloud is the mean key of each block, averaged over the lanes too:
  *
- *   C[b][d] = ( sum_{l=0}^{L-1} ( sum_{t=0}^{block-1} K[l][b*block+t][d] ) ) / (block*L)
+ *   C[b][d] = ( sum_{l=0}^{L-1} ( sum_{t=0}^{n_b-1} K[l][b*block+t][d] ) ) / (n_b*L)
  *
  * with both sums taken in ascending order, one binary64 accumulator each, and
- * one correctly rounded division at the end.
+ * one correctly rounded division at the end.  There are nb = ceil(S / block)
+ * blocks; n_b = block except for a partial last block, which holds the
+ * S - (nb-1)*block tokens that exist (the pages do not say; the mean over the
+ * tokens a block holds is the plainest reading).
  */
 int oracle_centroids(const uint16_t *K, int dtype, int64_t L, int64_t S, int64_t D,
                      int64_t block, double *C)
 {
-    if (block <= 0 || S % block != 0) return 1;
+    if (block <= 0 || S <= 0) return 1;
     const double *tab = decode_table(dtype);
-    int64_t nb = S / block;
+    int64_t nb = (S + block - 1) / block;
     double *part = (double *)malloc(sizeof(double) * (size_t)D);
     double *total = (double *)malloc(sizeof(double) * (size_t)D);
     if (!part || !total) { free(part); free(total); return 2; }
-    const double denom = (double)(block * L);
     for (int64_t b = 0; b < nb; ++b) {
+        const int64_t n_b = (b + 1) * block <= S ? block : S - b * block;
+        const double denom = (double)(n_b * L);
         for (int64_t d = 0; d < D; ++d) total[d] = 0.0;
         for (int64_t l = 0; l < L; ++l) {
             for (int64_t d = 0; d < D; ++d) part[d] = 0.0;
-            for (int64_t t = 0; t < block; ++t) {
+            for (int64_t t = 0; t < n_b; ++t) {
                 const uint16_t *row = K + ((l * S) + b * block + t) * D;
                 for (int64_t d = 0; d < D; ++d) part[d] = part[d] + tab[row[d]];
             }
@@ -391,8 +395,8 @@ int oracle_build_schedule_tie(const uint16_t *K, int dtype, int64_t L, int64_t S
                               int content, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
                               double *sal_sq)
 {
-    if (block <= 0 || S <= 0 || S % block != 0) return 1;
-    int64_t nb = S / block;
+    if (block <= 0 || S <= 0) return 1;
+    int64_t nb = (S + block - 1) / block;  /* a partial last block is a block too */
     double *C = (double *)malloc(sizeof(double) * (size_t)(nb * D));
     if (!C) return 2;
     int rc = oracle_centroids(K, dtype, L, S, D, block, C);
@@ -626,7 +630,8 @@ int oracle_attention_lse(const uint16_t *Q, const uint16_t *K, const uint16_t *V
                          int online, int nthreads)
 {
     if (lse && online) return 1;
-    if (block <= 0 || S % block != 0 || L <= 0 || D <= 0) return 1;
+    /* S need not be a multiple of block: keys k < S only (k <= q < S) */
+    if (block <= 0 || S <= 0 || L <= 0 || D <= 0) return 1;
     for (int64_t r = 0; r < n; ++r)
         if (lane[r] < 0 || lane[r] >= L || tok[r] < 0 || tok[r] >= S) return 1;
     if (nthreads < 1) nthreads = 1;
