@@ -51,7 +51,7 @@ typedef struct CUstream_st *tsa_stream_t;
 
 typedef enum {
     TSA_OK = 0,
-    TSA_ERR_INVALID_ARGUMENT = 1,  /* null pointer, non-positive size, S % block != 0, ...  */
+    TSA_ERR_INVALID_ARGUMENT = 1,  /* null pointer, non-positive size, misaligned, ...      */
     TSA_ERR_UNSUPPORTED = 2,       /* valid request this build does not implement          */
     TSA_ERR_NOT_DEVICE_POINTER = 3,/* a buffer is not device memory                        */
     TSA_ERR_DEVICE_MISMATCH = 4,   /* a buffer lives on another device than the current one */
@@ -69,9 +69,14 @@ const char *tsa_status_string(tsa_status status);
 
 /*
  * Upper bound on the nnz of a topology schedule:
- *   sum_{i=0}^{nb-1} min(i + 1, sink + local_radius + 1 + topk),  nb = S / block.
+ *   sum_{i=0}^{nb-1} min(i + 1, sink + local_radius + 1 + topk),  nb = ceil(S / block).
  * Size col_idx with at least this many entries for tsa_build_schedule.
- * Returns -1 for invalid arguments (S <= 0, block <= 0, S % block != 0, negative counts).
+ * Returns -1 for invalid arguments (S <= 0, block <= 0, negative counts).
+ *
+ * Partial last block (here and in tsa_build_schedule, tsa_dense_causal_csr and the attention
+ * forward): S need not be a multiple of the block.  There are nb = ceil(S / block) blocks; the
+ * last holds the S - (nb-1)*block tokens that exist, its centroid averages those tokens, and
+ * attention sees keys k < S only.  The pages do not say; this is the plainest reading.
  */
 int64_t tsa_schedule_max_nnz(int64_t S, int64_t block, int64_t sink, int64_t local_radius,
                              int64_t topk);
@@ -103,7 +108,7 @@ size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, i
  *   workspace    scratch of >= tsa_build_schedule_workspace_bytes(lanes, S, D, block) bytes,
  *                256-byte aligned; its contents on entry do not matter.
  *
- * Limits: 1 <= block, S % block == 0, 1 <= nb <= 4096, 1 <= D <= 1024, lanes >= 1.
+ * Limits: 1 <= block, 1 <= nb = ceil(S/block) <= 4096, 1 <= D <= 1024, lanes >= 1.
  * Errors: INVALID_ARGUMENT, NOT_DEVICE_POINTER, DEVICE_MISMATCH, CAPACITY, UNSUPPORTED
  * (nb or D beyond the limits), CUDA.  The result is bit-identical to the CPU oracle.
  */
@@ -208,8 +213,8 @@ tsa_status tsa_segment_csr(int64_t S, int64_t block, const int32_t *starts, int6
  * CSR layout"; Local benchmark: the dense CSR path visits every causal block):
  * row_ptr[i] = i(i+1)/2, row i = 0..i.  nnz = nb(nb+1)/2 (136 at nb 16, 2080 at nb 64).
  *
- *   row_ptr out, nb + 1 int32;  col_idx out, col_cap >= nb(nb+1)/2 int32.
- * Limits: S % block == 0, nb(nb+1)/2 < 2^31.  Errors: INVALID_ARGUMENT, CAPACITY,
+ *   row_ptr out, nb + 1 int32;  col_idx out, col_cap >= nb(nb+1)/2 int32 (nb = ceil(S/block)).
+ * Limits: nb(nb+1)/2 < 2^31.  Errors: INVALID_ARGUMENT, CAPACITY,
  * NOT_DEVICE_POINTER, DEVICE_MISMATCH, CUDA.
  */
 tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int32_t *col_idx,
@@ -228,9 +233,11 @@ tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int3
  *
  *   Q, K, V  in,  [B*H, S, D] of `dtype`, 16-byte aligned.
  *   O        out, same shape and dtype (must not alias Q, K or V).
- *   row_ptr, col_idx  the CSR (nb = S / 64 rows), on the device.
+ *   row_ptr, col_idx  the CSR (nb = ceil(S / 64) rows), on the device.
  *
- * Limits: block == 64, D in {64, 128}, S % 64 == 0, B*H <= 65535, B*H*S < 2^31.
+ * S need not be a multiple of 64: rows q >= S of a partial last block are neither computed
+ * into O nor into lse, and keys k >= S are never weighed.
+ * Limits: block == 64, D in {64, 128}, B*H <= 65535, B*H*S < 2^31.
  * Errors: INVALID_ARGUMENT, UNSUPPORTED (block or D), NOT_DEVICE_POINTER, DEVICE_MISMATCH,
  * CUDA.  Device-side: BAD_SCHEDULE (a row is truncated at its first bad entry), TIMEOUT.
  */
@@ -272,7 +279,8 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
  *                   256-byte aligned (Delta per row, the transposed schedule and its bitmap of
  *                   nb^2 bits); its contents on entry do not matter.
  *
- * Limits: block == 64, D in {64, 128}, S % 64 == 0, nb = S/64 <= 8192, B*H <= 65535,
+ * Limits: block == 64, D in {64, 128}, S % 64 == 0 (UNSUPPORTED otherwise: the backward pass
+ * needs whole blocks), nb = S/64 <= 8192, B*H <= 65535,
  * B*H*S < 2^31.  Errors: INVALID_ARGUMENT, UNSUPPORTED, CAPACITY (workspace), NOT_DEVICE_POINTER,
  * DEVICE_MISMATCH, CUDA.  Device-side: BAD_SCHEDULE (a row is cut at its first bad entry, as in
  * the forward), TSA_ERR_DEVICE (nnz above nnz_cap: dK and dV then come out zero), TIMEOUT.

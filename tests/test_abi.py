@@ -41,14 +41,15 @@ def test_max_nnz_closed_form():
     assert tsa.tsa_schedule_max_nnz(8192, 64, 1, 2, 4) == 996
     assert tsa.tsa_schedule_max_nnz(32768, 64, 2, 4, 8) == 7575
     assert tsa.tsa_schedule_max_nnz(1024, 64, 0, 100, 0) == 136
-    assert tsa.tsa_schedule_max_nnz(1000, 64, 1, 1, 2) == -1
+    assert tsa.tsa_schedule_max_nnz(1000, 64, 1, 1, 2) == 70  # a partial last block counts: 16 blocks
     assert tsa.tsa_schedule_max_nnz(1024, 64, -1, 1, 2) == -1
 
 
 def test_workspace_bytes():
     assert tsa.tsa_build_schedule_workspace_bytes(64, 32768, 128, 64) >= 64 * 512 * 128 * 8 + 512 * 512 * 8
     assert tsa.tsa_build_schedule_workspace_bytes(1, 64 * 4097, 64, 64) == 0  # beyond 4096 blocks
-    assert tsa.tsa_build_schedule_workspace_bytes(1, 100, 64, 64) == 0
+    assert tsa.tsa_build_schedule_workspace_bytes(1, 100, 64, 64) > 0  # 2 blocks, the last partial
+    assert tsa.tsa_build_schedule_workspace_bytes(1, 100, 64, 0) == 0
 
 
 def test_host_checks_before_any_device_call():
@@ -68,8 +69,8 @@ def test_host_checks_before_any_device_call():
     # unsupported block or head dimension
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 32, 0.1, None) == 2
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 96, 64, 0.1, None) == 2
-    # S not a multiple of the block, bad dtype, non-finite scale, misaligned pointer
-    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 100, 64, 64, 0.1, None) == 1
+    # empty sequence, bad dtype, non-finite scale, misaligned pointer
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 0, 64, 64, 0.1, None) == 1
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 5, 1, 1, 64, 64, 64, 0.1, None) == 1
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 64,
                                      float("nan"), None) == 1

@@ -53,7 +53,7 @@ def test_host_errors():
     k = torch.zeros((2, 256, 64), dtype=torch.float16, device=DEV)
     part = torch.zeros((2, 4, 64), dtype=torch.float64, device=DEV)
     assert L.tsa_block_sums(k.data_ptr(), 0, 2, 256, 64, 64, part.data_ptr() + 4, None) == 1  # misaligned
-    assert L.tsa_block_sums(k.data_ptr(), 0, 2, 250, 64, 64, part.data_ptr(), None) == 1      # S % block
+    assert L.tsa_block_sums(k.data_ptr(), 0, 2, 0, 64, 64, part.data_ptr(), None) == 1        # empty
     rp = torch.zeros(5, dtype=torch.int32, device=DEV)
     ci = torch.zeros(16, dtype=torch.int32, device=DEV)
     ws = torch.zeros(256, dtype=torch.uint8, device=DEV)

@@ -146,7 +146,7 @@ def tsa_build_schedule(K: torch.Tensor, block: int = 64, sink: int = 1, local_ra
     B, H, S, D = _lanes_S_D(K)
     lanes = B * H
     L = lib()
-    nb = S // block if block > 0 else 0
+    nb = -(-S // block) if block > 0 else 0  # a partial last block counts
     cap = int(L.tsa_schedule_max_nnz(S, block, sink, local_radius, topk))
     if cap < 0:
         raise TsaError(1, "tsa_schedule_max_nnz")
@@ -176,7 +176,7 @@ def tsa_block_sums(K: torch.Tensor, block: int = 64, *, out: torch.Tensor | None
         raise ValueError("K must be a contiguous CUDA tensor")
     B, H, S, D = _lanes_S_D(K)
     lanes = B * H
-    nb = S // block if block > 0 else 0
+    nb = -(-S // block) if block > 0 else 0  # a partial last block counts
     if out is None:
         out = torch.empty((lanes, nb, D), dtype=torch.float64, device=K.device)
     elif out.dtype != torch.float64 or not out.is_contiguous() or out.numel() != lanes * nb * D:
@@ -187,17 +187,22 @@ def tsa_block_sums(K: torch.Tensor, block: int = 64, *, out: torch.Tensor | None
 
 
 def tsa_build_schedule_from_sums(sums: torch.Tensor, block: int = 64, sink: int = 1, local_radius: int = 1,
-                                 topk: int = 2, *, salience: bool = False, tie_break: str = "index",
-                                 workspace: torch.Tensor | None = None, stream=None):
+                                 topk: int = 2, *, S: int | None = None, salience: bool = False,
+                                 tie_break: str = "index", workspace: torch.Tensor | None = None,
+                                 stream=None):
     """tsa_build_schedule from the block sums of all lanes ([lanes, nb, D] float64, lanes in
     global order, e.g. gathered from the GPUs that hold them).  Same result as
-    tsa_build_schedule on the full keys, bit for bit."""
+    tsa_build_schedule on the full keys, bit for bit.  S is the sequence length (default
+    nb * block; give it when the last block is partial)."""
     if not sums.is_cuda or not sums.is_contiguous() or sums.dtype != torch.float64 or sums.dim() != 3:
         raise ValueError("sums must be a contiguous CUDA float64 tensor [lanes, nb, D]")
     if tie_break not in TIE_RULES:
         raise ValueError(f"tie_break must be one of {sorted(TIE_RULES)}")
     lanes, nb, D = sums.shape
-    S = nb * block
+    if S is None:
+        S = nb * block
+    elif -(-S // block) != nb:
+        raise ValueError("S does not give sums.shape[1] blocks")
     L = lib()
     cap = int(L.tsa_schedule_max_nnz(S, block, sink, local_radius, topk))
     if cap < 0:
@@ -260,7 +265,7 @@ def tsa_segment_csr(S: int, block: int, starts: torch.Tensor, *, col_cap: int | 
 
 def tsa_dense_causal_csr(S: int, block: int = 64, device=None, stream=None):
     """Dense causal CSR (row i = blocks 0..i) as int32 device tensors."""
-    nb = S // block if block > 0 else 0
+    nb = -(-S // block) if block > 0 else 0  # a partial last block counts
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
     nnz = nb * (nb + 1) // 2

@@ -155,13 +155,13 @@ const char *tsa_status_string(tsa_status s) {
 
 int64_t tsa_schedule_max_nnz(int64_t S, int64_t block, int64_t sink, int64_t local_radius,
                              int64_t topk) {
-    if (S <= 0 || block <= 0 || S % block != 0 || sink < 0 || local_radius < 0 || topk < 0) return -1;
-    return max_nnz_bound(S / block, sink, local_radius, topk);
+    if (S <= 0 || block <= 0 || sink < 0 || local_radius < 0 || topk < 0) return -1;
+    return max_nnz_bound((S + block - 1) / block, sink, local_radius, topk);
 }
 
 size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, int64_t block) {
-    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return 0;
-    const int64_t nb = S / block;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0) return 0;
+    const int64_t nb = (S + block - 1) / block;
     if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return 0;
     return schedule_workspace_layout(lanes, nb, D).total;
 }
@@ -184,11 +184,11 @@ tsa_status tsa_build_schedule_ex(const void *K, tsa_dtype dtype, int64_t lanes, 
     if (!K || !row_ptr || !col_idx || !workspace) return TSA_ERR_INVALID_ARGUMENT;
     if (tie_break != TSA_TIE_INDEX && tie_break != TSA_TIE_CONTENT) return TSA_ERR_INVALID_ARGUMENT;
     if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
-    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
     if (sink < 0 || local_radius < 0 || topk < 0) return TSA_ERR_INVALID_ARGUMENT;
     if ((reinterpret_cast<uintptr_t>(K) & 1u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return TSA_ERR_INVALID_ARGUMENT;
-    const int64_t nb = S / block;
+    const int64_t nb = (S + block - 1) / block;  // a partial last block counts
     if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
     if (lanes > INT64_MAX / S / D) return TSA_ERR_INVALID_ARGUMENT;
     const int64_t need = max_nnz_bound(nb, sink, local_radius, topk);
@@ -228,10 +228,10 @@ tsa_status tsa_block_sums(const void *K, tsa_dtype dtype, int64_t lanes, int64_t
                           int64_t block, double *part, tsa_stream_t stream) {
     if (!K || !part) return TSA_ERR_INVALID_ARGUMENT;
     if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
-    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
     if ((reinterpret_cast<uintptr_t>(K) & 1u) || (reinterpret_cast<uintptr_t>(part) & 7u))
         return TSA_ERR_INVALID_ARGUMENT;
-    const int64_t nb = S / block;
+    const int64_t nb = (S + block - 1) / block;
     if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
     if (lanes > INT64_MAX / S / D) return TSA_ERR_INVALID_ARGUMENT;
     if (overlaps(part, (size_t)(lanes * nb * D) * 8, K, (size_t)(lanes * S * D) * 2)) return TSA_ERR_INVALID_ARGUMENT;
@@ -260,11 +260,11 @@ tsa_status tsa_build_schedule_from_sums(const double *part, int64_t lanes, int64
                                         tsa_stream_t stream) {
     if (!part || !row_ptr || !col_idx || !workspace) return TSA_ERR_INVALID_ARGUMENT;
     if (tie_break != TSA_TIE_INDEX && tie_break != TSA_TIE_CONTENT) return TSA_ERR_INVALID_ARGUMENT;
-    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
     if (sink < 0 || local_radius < 0 || topk < 0) return TSA_ERR_INVALID_ARGUMENT;
     if ((reinterpret_cast<uintptr_t>(part) & 7u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return TSA_ERR_INVALID_ARGUMENT;
-    const int64_t nb = S / block;
+    const int64_t nb = (S + block - 1) / block;
     if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
     if (lanes > INT64_MAX / nb / D / 8) return TSA_ERR_INVALID_ARGUMENT;
     const int64_t need = max_nnz_bound(nb, sink, local_radius, topk);
@@ -303,8 +303,8 @@ tsa_status tsa_build_schedule_from_sums(const double *part, int64_t lanes, int64
 tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int32_t *col_idx,
                                 int64_t col_cap, tsa_stream_t stream) {
     if (!row_ptr || !col_idx) return TSA_ERR_INVALID_ARGUMENT;
-    if (S <= 0 || block <= 0 || S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
-    const int64_t nb = S / block;
+    if (S <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = (S + block - 1) / block;
     if (nb > 65534) return TSA_ERR_INVALID_ARGUMENT;  // nb(nb+1)/2 must stay below 2^31
     if (col_cap < nb * (nb + 1) / 2) return TSA_ERR_CAPACITY;
     int dev;
@@ -373,7 +373,7 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
     if (block != 64 || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
-    if (S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    // S need not be a multiple of the block: the last query / key block may be partial
     if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
     const int64_t lanes = B * H;
     if (lanes * S >= (int64_t)INT_MAX) return TSA_ERR_UNSUPPORTED;
@@ -408,8 +408,9 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
     a.tmO = &tmO;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;
+    a.O = static_cast<uint16_t *>(O);
     a.lse = lse;
-    a.nb = (int)(S / block);
+    a.nb = (int)((S + block - 1) / block);
     a.S = (int)S;
     a.D = (int)D;
     a.lanes = (int)lanes;
@@ -439,7 +440,7 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0 || nnz_cap < 1) return TSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
     if (block != 64 || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
-    if (S % block != 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (S % block != 0) return TSA_ERR_UNSUPPORTED;  // the backward pass needs whole blocks
     if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
     const int64_t lanes = B * H, nb = S / block;
     if (lanes * S >= (int64_t)INT_MAX || nb > kMaxBackwardBlocks) return TSA_ERR_UNSUPPORTED;

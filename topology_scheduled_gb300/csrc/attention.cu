@@ -29,6 +29,10 @@
 //    any of its rows must (factor 1 for the others).
 //  * Epilogue.  O / l rounded to the input dtype, staged in the Q tile, TMA-stored per block;
 //    optionally the row's log-sum-exp (m + log l), which the backward pass recomputes P from.
+//  * Partial last block (S not a multiple of 64).  Its key rows past S are read but never
+//    weigh: the block is visited only as the diagonal block of the last row, where the causal
+//    mask already drops keys after the query token.  Its query rows past S are computed and
+//    dropped: the block's output is written row by row for the rows that exist.
 //  * Two CTAs share an SM, so one CTA's softmax also overlaps the other's MMAs.
 // Every mbarrier wait is bounded; on a timeout the CTA records TSA_ERR_TIMEOUT, drains its
 // in-flight copies and MMAs (bounded), frees TMEM and returns.
@@ -51,6 +55,7 @@ constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
 
 template <int D>
 struct AttnSmem {
+    static constexpr int kD = D;
     static constexpr int kChunks = D / 64;            // 64-element (128 B) column chunks
     static constexpr int kQBytes = kRows * D * 2;     // Q tile, later the O staging tile
     static constexpr int kKVBytes = kBlock * D * 2;   // one K or V tile
@@ -158,7 +163,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmV,
                            const __grid_constant__ CUtensorMap tmO,
                            const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
-                           float *__restrict__ lse_out, int nb, int S, float scale_log2, DeviceFlags flags) {
+                           uint16_t *__restrict__ O, float *__restrict__ lse_out, int nb, int S,
+                           float scale_log2, DeviceFlags flags) {
     using L = AttnSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -489,10 +495,14 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         if (*abort_flag == 0) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+            // A partial last query block (S not a multiple of 64) is not TMA-stored -- its box
+            // would run into the next lane's rows -- but written row by row from registers.
+            const int tok = qa * kBlock + tid;  // this thread's token (rows of both halves)
+            const bool partial = (my_block + 1) * kBlock > S;
+            const bool tok_ok = row_exists && tok < S;
             // log-sum-exp of the scaled scores in natural-log units, for the backward pass
-            if (lse_out && row_exists)
-                lse_out[row0 + qa * kBlock + tid] =
-                    l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
+            if (lse_out && tok_ok)
+                lse_out[row0 + tok] = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.6931471805599453f : -INFINITY;
             const uint32_t sw = (uint32_t)(tid & 7);
             __syncwarp();
 #pragma unroll
@@ -517,6 +527,9 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                 __uint_as_float(o[q * 8 + 2 * t + 1]) * inv, unused);
                         const uint32_t chunk16 = (uint32_t)(h * 4 + q);
                         st_shared_v4(o_row + ((chunk16 ^ sw) << 4), w[0], w[1], w[2], w[3]);
+                        if (partial && tok_ok)
+                            *reinterpret_cast<uint4 *>(O + ((size_t)row0 + tok) * L::kD + c * 64 + chunk16 * 8) =
+                                make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
             }
@@ -525,8 +538,9 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             if (tid == 0) {
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_store_2d(&tmO, c * 64, row0 + qa * kBlock, sQ + c * 16384);
-                    if (has_b) tma_store_2d(&tmO, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
+                    if ((qa + 1) * kBlock <= S) tma_store_2d(&tmO, c * 64, row0 + qa * kBlock, sQ + c * 16384);
+                    if (has_b && (qa + 2) * kBlock <= S)
+                        tma_store_2d(&tmO, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
                 }
                 tma_store_commit();
                 tma_store_wait_all();
@@ -561,7 +575,7 @@ tsa_status launch_one(const AttnLaunch &a) {
     const int npairs = (a.nb + 1) / 2;
     dim3 grid((unsigned)npairs, (unsigned)a.lanes);
     kern<<<grid, kThreads, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
-                                                            a.col_idx, a.lse, a.nb, a.S, a.scale_log2,
+                                                            a.col_idx, a.O, a.lse, a.nb, a.S, a.scale_log2,
                                                             a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }

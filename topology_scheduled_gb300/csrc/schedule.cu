@@ -137,6 +137,7 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
         const int64_t g = w % groups;
         const int64_t lb = w / groups;  // l * nb + b
         const int64_t l = lb / nb, b = lb % nb;
+        const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
         const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
         double *dst = part + lb * D + g * 8;
         if (fp32_path) {
@@ -162,7 +163,7 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
                 mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
             };
             int64_t t = 0;
-            for (; t + 8 <= block; t += 8) {
+            for (; t + 8 <= n; t += 8) {
                 uint4 v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + (t + u) * D));
@@ -174,7 +175,7 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
                     two_sum(3, v[u].w);
                 }
             }
-            for (; t < block; ++t) {
+            for (; t < n; ++t) {
                 const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
                 two_sum(0, v.x);
                 two_sum(1, v.y);
@@ -195,7 +196,7 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
                     const bool all_zero = amin == 0xFFFFu;
                     const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
                     dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
-                                           : column_sum_exact_slow(src + 2 * i + h, D, block, bf16, spread_limit);
+                                           : column_sum_exact_slow(src + 2 * i + h, D, n, bf16, spread_limit);
                 }
             }
             continue;
@@ -204,7 +205,7 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
 #pragma unroll
         for (int i = 0; i < 8; ++i) col_init(c[i]);
         int64_t t = 0;
-        for (; t + 8 <= block; t += 8) {
+        for (; t + 8 <= n; t += 8) {
             uint4 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + (t + u) * D));
@@ -218,7 +219,7 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
                 }
             }
         }
-        for (; t < block; ++t) {
+        for (; t < n; ++t) {
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -229,11 +230,11 @@ __global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16,
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            if (col_exact(c[i], bf16, block, spread_limit)) {
+            if (col_exact(c[i], bf16, n, spread_limit)) {
                 dst[i] = col_value(c[i], bf16);
             } else {
                 double acc = 0.0;
-                for (int64_t tt = 0; tt < block; ++tt) acc += widen(__ldg(src + tt * D + i), bf16);
+                for (int64_t tt = 0; tt < n; ++tt) acc += widen(__ldg(src + tt * D + i), bf16);
                 dst[i] = acc;
             }
         }
@@ -250,29 +251,33 @@ __global__ void centroid_partial_scalar(const uint16_t *__restrict__ K, bool bf1
         const int64_t d = w % D;
         const int64_t lb = w / D;
         const int64_t l = lb / nb, b = lb % nb;
+        const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
         const uint16_t *src = K + (l * S + b * block) * D + d;
         ColumnSum c;
         col_init(c);
-        for (int64_t t = 0; t < block; ++t) col_add(c, __ldg(src + t * D), bf16);
-        if (col_exact(c, bf16, block, spread_limit)) {
+        for (int64_t t = 0; t < n; ++t) col_add(c, __ldg(src + t * D), bf16);
+        if (col_exact(c, bf16, n, spread_limit)) {
             part[w] = col_value(c, bf16);
         } else {
             double acc = 0.0;
-            for (int64_t t = 0; t < block; ++t) acc += widen(__ldg(src + t * D), bf16);
+            for (int64_t t = 0; t < n; ++t) acc += widen(__ldg(src + t * D), bf16);
             part[w] = acc;
         }
     }
 }
 
-// C[b][d] = (sum_{l ascending} part[l][b][d]) / (block * lanes)
+// C[b][d] = (sum_{l ascending} part[l][b][d]) / (n_b * lanes), n_b the tokens block b holds
+// (block, or fewer for a partial last block).
 __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, int64_t nb,
-                               int64_t D, double denom, double *__restrict__ C) {
+                               int64_t D, int64_t S, int64_t block, double *__restrict__ C) {
     const int64_t n = nb * D;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n;
          w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = w / D;
+        const int64_t n_b = (b + 1) * block <= S ? block : S - b * block;
         double total = 0.0;
         for (int64_t l = 0; l < lanes; ++l) total += part[l * n + w];
-        C[w] = total / denom;
+        C[w] = total / (double)(n_b * lanes);
     }
 }
 
@@ -988,7 +993,7 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     {
         const int64_t n = a.nb * a.D;
         const unsigned g = (unsigned)((n + 255) / 256);
-        centroid_final<<<g, 256, 0, st>>>(sums, a.lanes, a.nb, a.D, (double)(a.block * a.lanes), cent);
+        centroid_final<<<g, 256, 0, st>>>(sums, a.lanes, a.nb, a.D, a.S, a.block, cent);
     }
     // content rule: rank the blocks, run the graph on the centroids in rank order
     int *perm = nullptr;

@@ -22,6 +22,7 @@ __host__ __device__ constexpr int kAttnSmemBytes() {
 struct AttnLaunch {
     const CUtensorMap *tmQ, *tmK, *tmV, *tmO;
     const int32_t *row_ptr, *col_idx;
+    uint16_t *O;  // the output (a partial last block is written with plain stores)
     float *lse;  // optional: natural-log log-sum-exp of the scaled scores per query row
     int nb, S, D, lanes;
     bool bf16;

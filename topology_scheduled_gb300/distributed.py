@@ -44,4 +44,4 @@ def build_schedule_lane_sharded(K_local: torch.Tensor, block: int = 64, sink: in
     (row_ptr, col_idx)."""
     sums = tsa_block_sums(K_local, block)
     return tsa_build_schedule_from_sums(gather_block_sums(sums, group), block, sink, local_radius, topk,
-                                        tie_break=tie_break)
+                                        S=K_local.shape[-2], tie_break=tie_break)
