@@ -126,7 +126,9 @@ __device__ double column_sum_exact_slow(const uint16_t *src, int64_t D, int64_t 
 // hi + lo is the exact column sum.  That sum has at most e_max - e_min + 14 <= 42 significant
 // bits, so the sequential binary64 sum is exact too and both equal (double)hi + (double)lo.
 // Other columns (and f16, and blocks longer than 64) take the int64 path above.
-__global__ void centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
+// Two CTAs of 256 threads per SM (at most 128 registers): this pass is bound by the HBM
+// read of K, and occupancy is what keeps enough loads in flight.
+__global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
                                       int64_t S, int64_t D, int64_t block, int64_t nb,
                                       int spread_limit, double *__restrict__ part) {
     const int64_t groups = D / 8;
