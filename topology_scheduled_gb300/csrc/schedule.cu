@@ -392,8 +392,9 @@ __global__ void __launch_bounds__(64) pairwise_d2(const double *__restrict__ C, 
 //     key (d2, min(u,v), max(u,v))); CTA 0 takes each component's lightest edge, hooks along
 //     it (a mutual pair keeps the smaller label as root), records each chosen edge once,
 //     flattens by pointer jumping and relabels.  The rounds stop at one component.
-//   Elder rule (CTA 0): bitonic sort of the nb-1 MST edges by the same key, then one thread
-//     merges in that order with a union-find in shared memory: the smaller component is
+//   Elder rule (CTA 0): bitonic sort of the nb-1 MST edges by the same key, then one warp
+//     merges in that order with a union-find in shared memory, 32 edges at a time (a prefix
+//     of merges whose components are disjoint is applied at once): the smaller component is
 //     absorbed (size tie: the root with the larger index) and its root receives the edge's d2.
 //   CSR: every CTA sorts the blocks by (salience desc, index asc); warps count each row's
 //     blocks from a per-row bitmap (sink range, local window, first topk blocks <= i of the
@@ -633,7 +634,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     unsigned long long *kd = reinterpret_cast<unsigned long long *>(sm);
     unsigned long long *kab = kd + pow2;
     volatile int *size = reinterpret_cast<volatile int *>(kab + pow2);
-    volatile int *label = size + nb;  // union-find parents
+    volatile int *label = size + nb;  // union-find parents, then the claims (nb each)
     const int ne = nb - 1;
     // under content ties the merges run on ranks: salience goes to a rank-indexed scratch and
     // is scattered to blocks at the end (one global write per merge, no dependent load)
@@ -670,46 +671,77 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     } else {
         bitonic_sort_pairs(kd, kab, pow2);
     }
-    // Merges in edge order, one thread, union-find in shared memory.  The smaller component is
+    // Merges in edge order with a union-find in shared memory.  The smaller component is
     // absorbed (on a size tie the root with the larger index), so linking the absorbed root
     // under the survivor is union by size: trees stay O(log nb) deep, path halving keeps them
     // flatter, and the root of a component is always its survivor -- the one block of it that
     // has received no merge distance yet.
-    if (threadIdx.x == 0) {
+    // One warp takes the edges 32 at a time: each lane finds its edge's two roots (finds only
+    // read parents or halve paths, so they may run together); the lanes whose roots no earlier
+    // lane of the group touches form a prefix of independent merges, applied at once; the
+    // group then resumes at the first lane that had to wait.  Same merges, same order of
+    // effect as one edge at a time, fewer rounds when consecutive edges join disjoint
+    // components.
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
         int *par = const_cast<int *>(label);
         int *siz = const_cast<int *>(size);
-        for (int e = 0; e < ne; ++e) {
-            const unsigned long long ab = kab[e];
-            const int x = (int)(ab >> 32), y = (int)(ab & 0xFFFFFFFFu);
-            if (x < 0 || x >= nb || y < 0 || y >= nb) {
-                raise_status(a.flags, kDevCapacity);
+        int *claim = par + nb;  // lowest lane of the group using a root (INT_MAX: none)
+        for (int v = lane; v < nb; v += 32) claim[v] = INT_MAX;
+        __syncwarp();
+        for (int e0 = 0; e0 < ne;) {
+            const int e = e0 + lane;
+            const bool has = e < ne;
+            int x = 0, y = 0;
+            if (has) {
+                const unsigned long long ab = kab[e];
+                x = (int)(ab >> 32);
+                y = (int)(ab & 0xFFFFFFFFu);
+            }
+            if (__any_sync(0xffffffffu, has && (x < 0 || x >= nb || y < 0 || y >= nb))) {
+                if (lane == 0) raise_status(a.flags, kDevCapacity);
                 break;
             }
             int rx = x, ry = y;
-            // both finds at once (independent loads overlap); at most nb steps each
-            for (int it = 0; it < nb; ++it) {
-                const int px = par[rx], py = par[ry];
-                if (px == rx && py == ry) break;
-                if (px != rx) {
-                    const int gx = par[px];
-                    par[rx] = gx;
-                    rx = gx;
+            if (has) {
+                for (int it = 0; it < nb; ++it) {  // both finds at once; at most nb steps
+                    const int px = par[rx], py = par[ry];
+                    if (px == rx && py == ry) break;
+                    if (px != rx) {
+                        const int gx = par[px];
+                        par[rx] = gx;
+                        rx = gx;
+                    }
+                    if (py != ry) {
+                        const int gy = par[py];
+                        par[ry] = gy;
+                        ry = gy;
+                    }
                 }
-                if (py != ry) {
-                    const int gy = par[py];
-                    par[ry] = gy;
-                    ry = gy;
-                }
+                atomicMin(&claim[rx], lane);
+                atomicMin(&claim[ry], lane);
             }
-            if (rx == ry) continue;  // cannot happen for MST edges
-            const int sx = siz[rx], sy = siz[ry];
-            int absorbed, survivor;
-            if (sx < sy) { absorbed = rx; survivor = ry; }
-            else if (sy < sx) { absorbed = ry; survivor = rx; }
-            else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
-            par[absorbed] = survivor;
-            siz[survivor] = sx + sy;
-            sal[absorbed] = __longlong_as_double((long long)kd[e]);
+            __syncwarp();
+            const bool wait = !has || claim[rx] != lane || claim[ry] != lane;
+            const unsigned wmask = __ballot_sync(0xffffffffu, wait);
+            const int k = wmask ? __ffs(wmask) - 1 : 32;  // lanes [0, k) merge now; k >= 1
+            if (lane < k && rx != ry) {  // rx == ry cannot happen for MST edges
+                const int sx = siz[rx], sy = siz[ry];
+                int absorbed, survivor;
+                if (sx < sy) { absorbed = rx; survivor = ry; }
+                else if (sy < sx) { absorbed = ry; survivor = rx; }
+                else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
+                par[absorbed] = survivor;
+                siz[survivor] = sx + sy;
+                sal[absorbed] = __longlong_as_double((long long)kd[e]);
+            }
+            __syncwarp();
+            if (has) {
+                claim[rx] = INT_MAX;
+                claim[ry] = INT_MAX;
+            }
+            __syncwarp();
+            e0 += k;
         }
     }
     __syncthreads();
@@ -1020,7 +1052,7 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     const int words = (nb + 31) / 32;
     constexpr int kGraphThreads = 512;
     const size_t merge_smem = (size_t)nb * (8 + 8 + 4 + 4);
-    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 8;
+    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 12;  // edges, sizes, parents, claims
     const size_t topk_smem = (size_t)pow2 * 20 + (size_t)(kGraphThreads / 32) * words * 4;
     size_t smem = merge_smem > elder_smem ? merge_smem : elder_smem;
     if (topk_smem > smem) smem = topk_smem;
