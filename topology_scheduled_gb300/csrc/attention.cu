@@ -92,17 +92,40 @@ static_assert(kMetaF + 4 * kMetaRing <= 256, "meta area");
 
 // Walks the union of two sorted CSR rows (query blocks qa and qa+1), checking the row
 // contract on the way.  Used by the producer thread.
+//
+// With 128-token blocks (coarse) the CTA's two 64-token query blocks are one CSR row p = qa/2,
+// and each 128-token key block j of it is visited as the 64-token blocks 2j and 2j+1: both
+// for both halves when j < p; on the diagonal (j == p) block 2p for both halves (the token
+// mask then holds keys to k <= q in the first half, the second half sees all of it) and block
+// 2p+1 for the second half only.  The allowed key set of every token is the 128-block one.
 struct RowUnion {
     const int32_t *col;
     int ia, ia_end, ib, ib_end;
     int last_a, last_b, qa, qb;
     bool bad;
+    bool coarse, has_b;
+    int nb64, pend, pend_flags;
 
-    __device__ void init(const int32_t *row_ptr, const int32_t *col_idx, int qa_, bool has_b) {
+    __device__ void init(const int32_t *row_ptr, const int32_t *col_idx, int qa_, bool has_b_,
+                         bool coarse_ = false, int nb64_ = 0) {
         col = col_idx;
         qa = qa_;
         qb = qa_ + 1;
         bad = false;
+        coarse = coarse_;
+        has_b = has_b_;
+        nb64 = nb64_;
+        pend = -1;
+        pend_flags = 0;
+        if (coarse) {
+            const int p = qa >> 1;
+            ia = row_ptr[p];
+            ia_end = row_ptr[p + 1];
+            if (ia_end - ia < 0 || ia_end - ia > p + 1) { bad = true; ia_end = ia; }
+            ib = ib_end = 0;
+            last_a = last_b = -1;
+            return;
+        }
         ia = row_ptr[qa];
         ia_end = row_ptr[qa + 1];
         if (ia_end - ia < 0 || ia_end - ia > qa + 1) { bad = true; ia_end = ia; }
@@ -118,6 +141,7 @@ struct RowUnion {
 
     // Next key block of the union and its membership bits (1: row qa, 2: row qb); -1 at end.
     __device__ int next(int &flags) {
+        if (coarse) return next_coarse(flags);
         int ja = INT_MAX, jb = INT_MAX;
         if (ia < ia_end) {
             ja = __ldg(col + ia);
@@ -133,6 +157,30 @@ struct RowUnion {
         if (ja == j) { last_a = ja; ++ia; }
         if (jb == j) { last_b = jb; ++ib; }
         return j;
+    }
+
+    // 64-token entries of a 128-token CSR row (see above).
+    __device__ int next_coarse(int &flags) {
+        if (pend >= 0) {
+            const int j = pend;
+            flags = pend_flags;
+            pend = -1;
+            return j;
+        }
+        const int p = qa >> 1;
+        if (ia >= ia_end) { flags = 0; return -1; }
+        const int j = __ldg(col + ia);
+        if (j <= last_a || j > p) { bad = true; ia_end = ia; flags = 0; return -1; }
+        last_a = j;
+        ++ia;
+        const int rows = has_b ? 3 : 1;
+        flags = rows;
+        const int fb = j < p ? rows : (rows & 2);
+        if (2 * j + 1 < nb64 && fb != 0) {
+            pend = 2 * j + 1;
+            pend_flags = fb;
+        }
+        return 2 * j;
     }
 };
 
@@ -164,7 +212,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmO,
                            const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
                            uint16_t *__restrict__ O, float *__restrict__ lse_out, int nb, int S,
-                           float scale_log2, DeviceFlags flags) {
+                           int coarse, float scale_log2, DeviceFlags flags) {
     using L = AttnSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -246,8 +294,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmO);
             RowUnion ruk, ruv;  // each stream walks the row union on its own
-            ruk.init(row_ptr, col_idx, qa, has_b);
-            ruv.init(row_ptr, col_idx, qa, has_b);
+            ruk.init(row_ptr, col_idx, qa, has_b, coarse != 0, nb);
+            ruv.init(row_ptr, col_idx, qa, has_b, coarse != 0, nb);
             mbar_arrive_expect_tx(bar_q, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
@@ -575,8 +623,8 @@ tsa_status launch_one(const AttnLaunch &a) {
     const int npairs = (a.nb + 1) / 2;
     dim3 grid((unsigned)npairs, (unsigned)a.lanes);
     kern<<<grid, kThreads, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
-                                                            a.col_idx, a.O, a.lse, a.nb, a.S, a.scale_log2,
-                                                            a.flags);
+                                                            a.col_idx, a.O, a.lse, a.nb, a.S, a.coarse ? 1 : 0,
+                                                            a.scale_log2, a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }
 

@@ -24,8 +24,9 @@ struct AttnLaunch {
     const int32_t *row_ptr, *col_idx;
     uint16_t *O;  // the output (a partial last block is written with plain stores)
     float *lse;  // optional: natural-log log-sum-exp of the scaled scores per query row
-    int nb, S, D, lanes;
+    int nb, S, D, lanes;  // nb: 64-token blocks
     bool bf16;
+    bool coarse;  // the CSR has 128-token blocks
     float scale_log2;
     DeviceFlags flags;
     cudaStream_t stream;
