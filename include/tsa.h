@@ -234,12 +234,14 @@ tsa_status tsa_dense_causal_csr(int64_t S, int64_t block, int32_t *row_ptr, int3
  *   Q, K, V  in,  [B*H, S, D] of `dtype`, 16-byte aligned.
  *   O        out, same shape and dtype (must not alias Q, K or V).
  *   row_ptr, col_idx  the CSR (nb = ceil(S / block) rows), on the device.
- *   block    64 or 128: the token block of the CSR (a 128-token block is walked as two 64-token
- *            ones; every token's allowed key set is the 128-block one).
+ *   block    32, 64 or 128: the token block of the CSR.  The kernel works in 64-token key steps:
+ *            a 128-token key block is walked as two, two 32-token key blocks share one with a
+ *            mask per (32-row query block, 32-key half); every token's allowed key set is the
+ *            one the CSR defines at its own block.
  *
  * S need not be a multiple of the block: rows q >= S of a partial last block are neither
  * computed into O nor into lse, and keys k >= S are never weighed.
- * Limits: block in {64, 128}, D in {64, 128}, B*H <= 65535, B*H*S < 2^31.
+ * Limits: block in {32, 64, 128}, D in {64, 128}, B*H <= 65535, B*H*S < 2^31.
  * Errors: INVALID_ARGUMENT, UNSUPPORTED (block or D), NOT_DEVICE_POINTER, DEVICE_MISMATCH,
  * CUDA.  Device-side: BAD_SCHEDULE (a row is truncated at its first bad entry), TIMEOUT.
  */

@@ -67,7 +67,7 @@ def test_host_checks_before_any_device_call():
     assert L.tsa_segment_csr(4096, 64, None, 3, fake, fake, 10, None) == 1  # starts missing
     assert L.tsa_segment_csr(4000, 64, None, 0, fake, fake, 10, None) == 1
     # unsupported block or head dimension
-    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 32, 0.1, None) == 2
+    assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 64, 16, 0.1, None) == 2
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 64, 96, 64, 0.1, None) == 2
     # empty sequence, bad dtype, non-finite scale, misaligned pointer
     assert L.tsa_scheduled_attention(fake, fake, fake, fake, fake, fake, 0, 1, 1, 0, 64, 64, 0.1, None) == 1

@@ -372,7 +372,7 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
     if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
-    if ((block != 64 && block != 128) || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
+    if ((block != 32 && block != 64 && block != 128) || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
     // S need not be a multiple of the block: the last query / key block may be partial
     if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
     const int64_t lanes = B * H;
@@ -411,7 +411,7 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
     a.O = static_cast<uint16_t *>(O);
     a.lse = lse;
     a.nb = (int)((S + 63) / 64);  // the kernel works in 64-token blocks
-    a.coarse = block == 128;
+    a.gran = block == 128 ? 1 : block == 32 ? 2 : 0;
     a.S = (int)S;
     a.D = (int)D;
     a.lanes = (int)lanes;

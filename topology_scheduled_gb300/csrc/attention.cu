@@ -184,6 +184,94 @@ struct RowUnion {
     }
 };
 
+// 32-token blocks: the CTA's 128 rows are query blocks r0 .. r0+3 (r0 = 2 qa), and each 64-token
+// key block k of the union of their CSR rows carries one bit per (query quarter r, key half h):
+// bit 2r + h when row r0 + r holds 32-token key block 2k + h.  Rows are checked as above.
+struct RowUnion32 {
+    const int32_t *col;
+    int pos[4], end[4], last[4];
+    int r0;
+    bool bad;
+
+    __device__ void init(const int32_t *row_ptr, const int32_t *col_idx, int r0_, int nrows) {
+        col = col_idx;
+        r0 = r0_;
+        bad = false;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            last[r] = -1;
+            pos[r] = end[r] = 0;
+            if (r < nrows) {
+                pos[r] = row_ptr[r0 + r];
+                end[r] = row_ptr[r0 + r + 1];
+                if (end[r] - pos[r] < 0 || end[r] - pos[r] > r0 + r + 1) { bad = true; end[r] = pos[r]; }
+            }
+        }
+    }
+
+    __device__ int head(int r) {
+        if (pos[r] >= end[r]) return INT_MAX;
+        const int x = __ldg(col + pos[r]);
+        if (x <= last[r] || x > r0 + r) { bad = true; end[r] = pos[r]; return INT_MAX; }
+        return x;
+    }
+
+    __device__ int next(int &flags) {
+        int h[4], j = INT_MAX;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            h[r] = head(r);
+            j = h[r] < j ? h[r] : j;
+        }
+        flags = 0;
+        if (j == INT_MAX) return -1;
+        const int k = j >> 1;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (h[r] == 2 * k + hh) {
+                    flags |= 1 << (2 * r + hh);
+                    last[r] = h[r];
+                    ++pos[r];
+                    h[r] = head(r);
+                }
+            }
+        }
+        return k;
+    }
+};
+
+// The producer's walk for any block size: entries are 64-token key blocks with 8 membership
+// bits, bit 2r + h for query quarter r (rows 32r .. 32r+31 of the CTA) and key half h.
+struct EntryWalk {
+    RowUnion u;
+    RowUnion32 u32;
+    bool fine;
+
+    __device__ void init(const int32_t *row_ptr, const int32_t *col_idx, int qa, bool has_b, int gran,
+                         int nb64, int S) {
+        fine = gran == 2;
+        if (fine) {
+            const int nb32 = (S + 31) / 32;
+            const int r0 = 2 * qa;
+            u32.init(row_ptr, col_idx, r0, nb32 - r0 < 4 ? nb32 - r0 : 4);
+        } else {
+            u.init(row_ptr, col_idx, qa, has_b, gran == 1, nb64);
+        }
+    }
+
+    __device__ int next(int &flags) {
+        if (fine) return u32.next(flags);
+        int f = 0;
+        const int j = u.next(f);
+        flags = ((f & 1) ? 0x0F : 0) | ((f & 2) ? 0xF0 : 0);  // a 64-token half is two quarters
+        return j;
+    }
+
+    __device__ bool bad() const { return fine ? u32.bad : u.bad; }
+};
+
 // Two floats rounded to the 16-bit input dtype, packed (first in the low half); `sum` gets
 // the rounded values.
 template <bool kBF16>
@@ -212,7 +300,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmO,
                            const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
                            uint16_t *__restrict__ O, float *__restrict__ lse_out, int nb, int S,
-                           int coarse, float scale_log2, DeviceFlags flags) {
+                           int gran, float scale_log2, DeviceFlags flags) {
     using L = AttnSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -293,9 +381,9 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmO);
-            RowUnion ruk, ruv;  // each stream walks the row union on its own
-            ruk.init(row_ptr, col_idx, qa, has_b, coarse != 0, nb);
-            ruv.init(row_ptr, col_idx, qa, has_b, coarse != 0, nb);
+            EntryWalk ruk, ruv;  // each stream walks the row union on its own
+            ruk.init(row_ptr, col_idx, qa, has_b, gran, nb, S);
+            ruv.init(row_ptr, col_idx, qa, has_b, gran, nb, S);
             mbar_arrive_expect_tx(bar_q, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
@@ -355,7 +443,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     }
                 }
             }
-            if (ruk.bad) raise_status(flags, kDevBadSchedule);
+            if (ruk.bad()) raise_status(flags, kDevBadSchedule);
             if (!ok) {
                 // Drain: wait (bounded) for every load issued into the rings.
                 *abort_flag = 1;
@@ -440,7 +528,6 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     } else {
         // ------------------------------------------------------------ softmax (warps 0-3)
         const int half = tid >> 6;               // 0: block qa, 1: block qa+1
-        const int r_in = tid & 63;               // token within the query block
         const int my_block = qa + half;
         const bool row_exists = half == 0 || has_b;
         const uint32_t t_lane = (uint32_t)(warp * 32) << 16;  // this warp's TMEM lane quarter
@@ -454,7 +541,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             const int fl = meta_f[u % kMetaRing];
             if (j < 0) break;
             tc_fence_after();
-            const bool in_row = row_exists && ((fl >> half) & 1);  // warp-uniform
+            const int fq = (fl >> (2 * warp)) & 3;  // key halves this warp's 32 rows hold
+            const bool in_row = row_exists && fq != 0;  // warp-uniform
             const uint32_t s_addr = tmem + t_lane + s_col(u & 1);
             uint32_t pw[32];
             __syncwarp();
@@ -464,10 +552,16 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 float x[64];  // raw scores q.k
 #pragma unroll
                 for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-                if (j == my_block) {  // diagonal block: keys after the query token are masked
+                if (fq != 3) {  // a 32-token key half the row does not hold (32-token blocks)
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (c > r_in) x[c] = -INFINITY;
+                        if (!((fq >> (c >> 5)) & 1)) x[c] = -INFINITY;
+                }
+                if (j >= qa) {  // near the diagonal: keys after the query token are masked
+                    const int lim = (qa - j) * kBlock + tid;  // key 64j + c > query 64qa + tid
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c > lim) x[c] = -INFINITY;
                 }
                 float m21[22];
 #pragma unroll
@@ -623,7 +717,7 @@ tsa_status launch_one(const AttnLaunch &a) {
     const int npairs = (a.nb + 1) / 2;
     dim3 grid((unsigned)npairs, (unsigned)a.lanes);
     kern<<<grid, kThreads, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
-                                                            a.col_idx, a.O, a.lse, a.nb, a.S, a.coarse ? 1 : 0,
+                                                            a.col_idx, a.O, a.lse, a.nb, a.S, a.gran,
                                                             a.scale_log2, a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }

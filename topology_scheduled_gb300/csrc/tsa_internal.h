@@ -26,7 +26,7 @@ struct AttnLaunch {
     float *lse;  // optional: natural-log log-sum-exp of the scaled scores per query row
     int nb, S, D, lanes;  // nb: 64-token blocks
     bool bf16;
-    bool coarse;  // the CSR has 128-token blocks
+    int gran;  // token block of the CSR: 0 for 64, 1 for 128, 2 for 32
     float scale_log2;
     DeviceFlags flags;
     cudaStream_t stream;
