@@ -141,7 +141,6 @@ struct RowUnion {
 
     // Next key block of the union and its membership bits (1: row qa, 2: row qb); -1 at end.
     __device__ int next(int &flags) {
-        if (coarse) return next_coarse(flags);
         int ja = INT_MAX, jb = INT_MAX;
         if (ia < ia_end) {
             ja = __ldg(col + ia);
@@ -242,34 +241,34 @@ struct RowUnion32 {
     }
 };
 
-// The producer's walk for any block size: entries are 64-token key blocks with 8 membership
-// bits, bit 2r + h for query quarter r (rows 32r .. 32r+31 of the CTA) and key half h.
+// The producer's walk for the CSR's block size kGran (0: 64, 1: 128, 2: 32 tokens): entries are
+// 64-token key blocks with their membership bits -- with 32-token blocks bit 2r + h per (query
+// quarter r, key half h), otherwise bit h per 64-row query half h (the whole 64-key step).
+template <int kGran>
 struct EntryWalk {
     RowUnion u;
     RowUnion32 u32;
-    bool fine;
 
-    __device__ void init(const int32_t *row_ptr, const int32_t *col_idx, int qa, bool has_b, int gran,
-                         int nb64, int S) {
-        fine = gran == 2;
-        if (fine) {
+    __device__ void init(const int32_t *row_ptr, const int32_t *col_idx, int qa, bool has_b, int nb64, int S) {
+        if constexpr (kGran == 2) {
             const int nb32 = (S + 31) / 32;
             const int r0 = 2 * qa;
             u32.init(row_ptr, col_idx, r0, nb32 - r0 < 4 ? nb32 - r0 : 4);
         } else {
-            u.init(row_ptr, col_idx, qa, has_b, gran == 1, nb64);
+            u.init(row_ptr, col_idx, qa, has_b, kGran == 1, nb64);
         }
     }
 
     __device__ int next(int &flags) {
-        if (fine) return u32.next(flags);
-        int f = 0;
-        const int j = u.next(f);
-        flags = ((f & 1) ? 0x0F : 0) | ((f & 2) ? 0xF0 : 0);  // a 64-token half is two quarters
-        return j;
+        if constexpr (kGran == 2) return u32.next(flags);
+        else if constexpr (kGran == 1) return u.next_coarse(flags);
+        else return u.next(flags);
     }
 
-    __device__ bool bad() const { return fine ? u32.bad : u.bad; }
+    __device__ bool bad() const {
+        if constexpr (kGran == 2) return u32.bad;
+        else return u.bad;
+    }
 };
 
 // Two floats rounded to the 16-bit input dtype, packed (first in the low half); `sum` gets
@@ -292,7 +291,7 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, float &sum) {
 static_assert(AttnSmem<128>::kOffMeta + AttnSmem<128>::kMetaBytes + 512 <= kAttnSmemBytes<128>(), "smem");
 static_assert(AttnSmem<64>::kOffMeta + AttnSmem<64>::kMetaBytes + 512 <= kAttnSmemBytes<64>(), "smem");
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, int kGran>
 __global__ void __launch_bounds__(kThreads, 2)
 scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmK,
@@ -300,7 +299,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                            const __grid_constant__ CUtensorMap tmO,
                            const int32_t *__restrict__ row_ptr, const int32_t *__restrict__ col_idx,
                            uint16_t *__restrict__ O, float *__restrict__ lse_out, int nb, int S,
-                           int gran, float scale_log2, DeviceFlags flags) {
+                           float scale_log2, DeviceFlags flags) {
+    constexpr bool kFine = kGran == 2;  // 32-token blocks: masks per (query quarter, key half)
     using L = AttnSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
@@ -381,9 +381,9 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmO);
-            EntryWalk ruk, ruv;  // each stream walks the row union on its own
-            ruk.init(row_ptr, col_idx, qa, has_b, gran, nb, S);
-            ruv.init(row_ptr, col_idx, qa, has_b, gran, nb, S);
+            EntryWalk<kGran> ruk, ruv;  // each stream walks the row union on its own
+            ruk.init(row_ptr, col_idx, qa, has_b, nb, S);
+            ruv.init(row_ptr, col_idx, qa, has_b, nb, S);
             mbar_arrive_expect_tx(bar_q, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
@@ -541,7 +541,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             const int fl = meta_f[u % kMetaRing];
             if (j < 0) break;
             tc_fence_after();
-            const int fq = (fl >> (2 * warp)) & 3;  // key halves this warp's 32 rows hold
+            // key halves this warp's 32 rows hold (both, with 64- or 128-token blocks)
+            const int fq = kFine ? (fl >> (2 * warp)) & 3 : ((fl >> half) & 1) * 3;
             const bool in_row = row_exists && fq != 0;  // warp-uniform
             const uint32_t s_addr = tmem + t_lane + s_col(u & 1);
             uint32_t pw[32];
@@ -552,16 +553,22 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 float x[64];  // raw scores q.k
 #pragma unroll
                 for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sr[c >> 5][c & 31]);
-                if (fq != 3) {  // a 32-token key half the row does not hold (32-token blocks)
+                if constexpr (kFine) {
+                    if (fq != 3) {  // a 32-token key half this row does not hold
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (!((fq >> (c >> 5)) & 1)) x[c] = -INFINITY;
+                    }
+                    if (j >= qa) {  // near the diagonal: keys after the query token are masked
+                        const int lim = (qa - j) * kBlock + tid;  // key 64j + c > query 64qa + tid
+#pragma unroll
+                        for (int c = 0; c < 64; ++c)
+                            if (c > lim) x[c] = -INFINITY;
+                    }
+                } else if (j == my_block) {  // diagonal block: keys after the query token are masked
 #pragma unroll
                     for (int c = 0; c < 64; ++c)
-                        if (!((fq >> (c >> 5)) & 1)) x[c] = -INFINITY;
-                }
-                if (j >= qa) {  // near the diagonal: keys after the query token are masked
-                    const int lim = (qa - j) * kBlock + tid;  // key 64j + c > query 64qa + tid
-#pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        if (c > lim) x[c] = -INFINITY;
+                        if (c > (tid & 63)) x[c] = -INFINITY;
                 }
                 float m21[22];
 #pragma unroll
@@ -708,26 +715,31 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     }
 }
 
-template <int D, bool kBF16>
+template <int D, bool kBF16, int kGran>
 tsa_status launch_one(const AttnLaunch &a) {
-    auto kern = scheduled_attention_kernel<D, kBF16>;
+    auto kern = scheduled_attention_kernel<D, kBF16, kGran>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAttnSmemBytes<D>()) !=
         cudaSuccess)
         return TSA_ERR_CUDA;
     const int npairs = (a.nb + 1) / 2;
     dim3 grid((unsigned)npairs, (unsigned)a.lanes);
     kern<<<grid, kThreads, kAttnSmemBytes<D>(), a.stream>>>(*a.tmQ, *a.tmK, *a.tmV, *a.tmO, a.row_ptr,
-                                                            a.col_idx, a.O, a.lse, a.nb, a.S, a.gran,
+                                                            a.col_idx, a.O, a.lse, a.nb, a.S,
                                                             a.scale_log2, a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
+}
+
+template <int kGran>
+tsa_status launch_gran(const AttnLaunch &a) {
+    if (a.D == 64) return a.bf16 ? launch_one<64, true, kGran>(a) : launch_one<64, false, kGran>(a);
+    if (a.D == 128) return a.bf16 ? launch_one<128, true, kGran>(a) : launch_one<128, false, kGran>(a);
+    return TSA_ERR_UNSUPPORTED;
 }
 
 }  // namespace
 
 tsa_status launch_scheduled_attention(const AttnLaunch &a) {
-    if (a.D == 64) return a.bf16 ? launch_one<64, true>(a) : launch_one<64, false>(a);
-    if (a.D == 128) return a.bf16 ? launch_one<128, true>(a) : launch_one<128, false>(a);
-    return TSA_ERR_UNSUPPORTED;
+    return a.gran == 2 ? launch_gran<2>(a) : a.gran == 1 ? launch_gran<1>(a) : launch_gran<0>(a);
 }
 
 }  // namespace tsa
