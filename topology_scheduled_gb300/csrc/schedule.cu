@@ -634,7 +634,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     unsigned long long *kd = reinterpret_cast<unsigned long long *>(sm);
     unsigned long long *kab = kd + pow2;
     volatile int *size = reinterpret_cast<volatile int *>(kab + pow2);
-    volatile int *label = size + nb;  // union-find parents, then the claims (nb each)
+    volatile int *label = size + nb;  // union-find parents, then two claim arrays (nb each)
     const int ne = nb - 1;
     // under content ties the merges run on ranks: salience goes to a rank-indexed scratch and
     // is scattered to blocks at the end (one global write per merge, no dependent load)
@@ -677,17 +677,24 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
     // flatter, and the root of a component is always its survivor -- the one block of it that
     // has received no merge distance yet.
     // One warp takes the edges 32 at a time: each lane finds its edge's two roots (finds only
-    // read parents or halve paths, so they may run together); the lanes whose roots no earlier
-    // lane of the group touches form a prefix of independent merges, applied at once; the
-    // group then resumes at the first lane that had to wait.  Same merges, same order of
-    // effect as one edge at a time, fewer rounds when consecutive edges join disjoint
-    // components.
+    // read parents or halve paths, so they may run together) and decides its merge from the
+    // component sizes before the group.  A prefix of the group merges at once: lane l joins it
+    // when no earlier lane touches the root l absorbs, and no earlier lane absorbs the root l
+    // keeps.  A root shared by several of those lanes is then the survivor of each of their
+    // merges; it only grows, so every decision is the one taken edge by edge, and the
+    // absorbed roots are distinct.  (This covers a large component taking singletons one
+    // edge after another, as well as merges of disjoint components.)  The group resumes at
+    // the first lane that had to wait, which is never lane 0.
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
         int *par = const_cast<int *>(label);
         int *siz = const_cast<int *>(size);
-        int *claim = par + nb;  // lowest lane of the group using a root (INT_MAX: none)
-        for (int v = lane; v < nb; v += 32) claim[v] = INT_MAX;
+        int *used = par + nb;      // lowest lane of the group using a root (INT_MAX: none)
+        int *taken = used + nb;    // lowest lane of the group absorbing a root
+        for (int v = lane; v < nb; v += 32) {
+            used[v] = INT_MAX;
+            taken[v] = INT_MAX;
+        }
         __syncwarp();
         for (int e0 = 0; e0 < ne;) {
             const int e = e0 + lane;
@@ -718,27 +725,35 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
                         ry = gy;
                     }
                 }
-                atomicMin(&claim[rx], lane);
-                atomicMin(&claim[ry], lane);
+            }
+            int absorbed = 0, survivor = 0, sa = 0;
+            if (has && rx != ry) {  // rx == ry cannot happen for MST edges
+                const int sx = siz[rx], sy = siz[ry];
+                if (sx < sy) { absorbed = rx; survivor = ry; sa = sx; }
+                else if (sy < sx) { absorbed = ry; survivor = rx; sa = sy; }
+                else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; sa = sx; }
+                atomicMin(&used[absorbed], lane);
+                atomicMin(&used[survivor], lane);
+                atomicMin(&taken[absorbed], lane);
             }
             __syncwarp();
-            const bool wait = !has || claim[rx] != lane || claim[ry] != lane;
-            const unsigned wmask = __ballot_sync(0xffffffffu, wait);
+            // lane 0 is always ready (it is the lowest lane on both of its roots), so every round
+            // merges at least one edge; an edge inside one component (impossible for MST edges)
+            // is a ready no-op
+            const bool ready = has && (rx == ry || (used[absorbed] == lane && taken[survivor] > lane));
+            const unsigned wmask = __ballot_sync(0xffffffffu, !ready && has);
             const int k = wmask ? __ffs(wmask) - 1 : 32;  // lanes [0, k) merge now; k >= 1
-            if (lane < k && rx != ry) {  // rx == ry cannot happen for MST edges
-                const int sx = siz[rx], sy = siz[ry];
-                int absorbed, survivor;
-                if (sx < sy) { absorbed = rx; survivor = ry; }
-                else if (sy < sx) { absorbed = ry; survivor = rx; }
-                else { absorbed = rx > ry ? rx : ry; survivor = rx > ry ? ry : rx; }
+            __syncwarp();
+            if (lane < k && has && rx != ry) {
                 par[absorbed] = survivor;
-                siz[survivor] = sx + sy;
+                atomicAdd(&siz[survivor], sa);
                 sal[absorbed] = __longlong_as_double((long long)kd[e]);
             }
             __syncwarp();
-            if (has) {
-                claim[rx] = INT_MAX;
-                claim[ry] = INT_MAX;
+            if (has && rx != ry) {
+                used[absorbed] = INT_MAX;
+                used[survivor] = INT_MAX;
+                taken[absorbed] = INT_MAX;
             }
             __syncwarp();
             e0 += k;
@@ -1052,7 +1067,7 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     const int words = (nb + 31) / 32;
     constexpr int kGraphThreads = 512;
     const size_t merge_smem = (size_t)nb * (8 + 8 + 4 + 4);
-    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 12;  // edges, sizes, parents, claims
+    const size_t elder_smem = (size_t)pow2 * 16 + (size_t)nb * 16;  // edges, sizes, parents, 2 claims
     const size_t topk_smem = (size_t)pow2 * 20 + (size_t)(kGraphThreads / 32) * words * 4;
     size_t smem = merge_smem > elder_smem ? merge_smem : elder_smem;
     if (topk_smem > smem) smem = topk_smem;
