@@ -243,6 +243,113 @@ __global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *
     }
 }
 
+// The bf16 fast path of centroid_partial_vec8 (same items, same TwoSum arithmetic in the same
+// token order, so the same bits), streamed: each thread copies its next 8 rows of 16 bytes into
+// shared memory with cp.async while it sums earlier ones, so a thread always has loads in
+// flight instead of alternating between loading and summing.  The staging area is
+// [stage][row][thread] (16-byte words), so the 32 lanes of a warp touch consecutive words.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kStreamThreads = 256;
+constexpr int kStreamStages = 3;
+constexpr int kStreamSmem = kStreamStages * 8 * kStreamThreads * 16;  // 96 KB
+
+__global__ void __launch_bounds__(kStreamThreads, 2)
+centroid_partial_bf16_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S, int64_t D,
+                             int64_t block, int64_t nb, int spread_limit, double *__restrict__ part) {
+    extern __shared__ __align__(16) uint4 stage[];
+    const uint32_t stage0 = smem_u32(stage) + threadIdx.x * 16u;
+    const int64_t groups = D / 8;
+    const int64_t total = lanes * nb * groups;
+    for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
+         w += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = w % groups;
+        const int64_t lb = w / groups;  // l * nb + b
+        const int64_t l = lb / nb, b = lb % nb;
+        const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
+        const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
+        double *dst = part + lb * D + g * 8;
+        uint64_t hi[4], lo[4];
+        uint32_t mx[4], mn[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            hi[i] = f2_pack(0.f, 0.f);
+            lo[i] = hi[i];
+            mx[i] = 0u;
+            mn[i] = 0xFFFFFFFFu;
+        }
+        auto two_sum = [&](int i, uint32_t x) {
+            const uint64_t v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+            const uint64_t s = f2_add(hi[i], v);
+            const uint64_t bv = f2_sub(s, hi[i]);
+            const uint64_t err = f2_add(f2_sub(hi[i], f2_sub(s, bv)), f2_sub(v, bv));
+            lo[i] = f2_add(lo[i], err);
+            hi[i] = s;
+            const uint32_t a = x & 0x7FFF7FFFu;
+            mx[i] = __vmaxu2(mx[i], a);
+            mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
+        };
+        const int64_t chunks = n >> 3;  // whole chunks of 8 tokens
+        const int64_t full = chunks << 3;
+        // Ring of kStreamStages chunks; one commit group per chunk slot (empty past the end), so
+        // wait_group<kStreamStages - 1> always means "chunk c has landed".
+        auto issue = [&](int64_t c) {
+            if (c < chunks) {
+                const int buf = (int)(c % kStreamStages);
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    cp_async16(stage0 + (uint32_t)((buf * 8 + u) * kStreamThreads * 16), src + (c * 8 + u) * D);
+            }
+            cp_async_commit();
+        };
+#pragma unroll
+        for (int c = 0; c < kStreamStages - 1; ++c) issue(c);
+        for (int64_t c = 0; c < chunks; ++c) {
+            issue(c + kStreamStages - 1);
+            cp_async_wait<kStreamStages - 1>();
+            const int buf = (int)(c % kStreamStages);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint4 v = stage[(buf * 8 + u) * kStreamThreads + threadIdx.x];
+                two_sum(0, v.x);
+                two_sum(1, v.y);
+                two_sum(2, v.z);
+                two_sum(3, v.w);
+            }
+        }
+        cp_async_wait<0>();
+        for (int64_t t = full; t < n; ++t) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
+            two_sum(0, v.x);
+            two_sum(1, v.y);
+            two_sum(2, v.z);
+            two_sum(3, v.w);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float h0, h1, l0, l1;
+            f2_unpack(hi[i], h0, h1);
+            f2_unpack(lo[i], l0, l1);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
+                const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
+                const int emax = (int)(amax >> 7);
+                const int emin = max(1, (int)(amin >> 7));
+                const bool all_zero = amin == 0xFFFFu;
+                const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
+                dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
+                                       : column_sum_exact_slow(src + 2 * i + h, D, n, true, spread_limit);
+            }
+        }
+    }
+}
+
 // Same sums, one d per thread (any D, any alignment).
 __global__ void centroid_partial_scalar(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
                                         int64_t S, int64_t D, int64_t block, int64_t nb,
@@ -1001,7 +1108,13 @@ tsa_status launch_block_sums(const ScheduleLaunch &a, double *part) {
     int log2_block = 0;
     while ((int64_t(1) << log2_block) < a.block) ++log2_block;
     const int spread_limit = 45 - log2_block;
-    if (vec)
+    if (vec && a.bf16) {
+        if (cudaFuncSetAttribute(centroid_partial_bf16_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kStreamSmem) != cudaSuccess)
+            return TSA_ERR_CUDA;
+        centroid_partial_bf16_stream<<<grid, kStreamThreads, kStreamSmem, st>>>(a.K, a.lanes, a.S, a.D, a.block,
+                                                                                a.nb, spread_limit, part);
+    } else if (vec)
         centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
                                                         spread_limit, part);
     else
