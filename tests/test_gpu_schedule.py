@@ -153,3 +153,26 @@ def test_centroid_sums_with_extreme_exponents(dtype):
     x[:, :64, :8] = 1e-30  # columns of tiny values only (f16: zero, bf16: below the window)
     k = x.to(dtype).to(DEV)
     _assert_same(_gpu_schedule(k, 64, 1, 2, 3), _oracle_schedule(k, 64, 1, 2, 3), distinct=False)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("lanes,S", [(1, 1000), (16, 40000 - 23)])
+def test_block_sums_small_and_large_grids(dtype, lanes, S):
+    """Block sums against the sequential binary64 sum (tokens ascending) on a few CTAs (one
+    64-row block in flight per thread) and on a many-wave grid (a ring of 8-row chunks), with
+    columns whose exponents spread past the fast paths' bounds and a partial last block."""
+    D, block = 64, 64
+    g = torch.Generator().manual_seed(lanes + S)
+    x = torch.randn((lanes, S, D), generator=g)
+    lo_e, hi_e = (-24, 12) if dtype == torch.bfloat16 else (-20, 8)
+    x = x * torch.pow(2.0, torch.randint(lo_e, hi_e, (lanes, S, D), generator=g).float())
+    k = x.to(dtype)
+    got = tsa.tsa_block_sums(k.to(DEV), block).cpu().numpy()
+    nb = -(-S // block)
+    xd = np.zeros((lanes, nb * block, D))
+    xd[:, :S] = k.double().numpy()
+    xd = xd.reshape(lanes, nb, block, D)
+    ref = np.zeros((lanes, nb, D))
+    for t in range(block):
+        ref = ref + xd[:, :, t, :]  # padding rows add +0.0, which leaves a sum unchanged
+    assert np.array_equal(got, ref)

@@ -243,11 +243,12 @@ __global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *
     }
 }
 
-// The bf16 fast path of centroid_partial_vec8 (same items, same TwoSum arithmetic in the same
-// token order, so the same bits), streamed: each thread copies its next 8 rows of 16 bytes into
-// shared memory with cp.async while it sums earlier ones, so a thread always has loads in
-// flight instead of alternating between loading and summing.  The staging area is
+// centroid_partial_vec8's arithmetic (same items, same per-column arithmetic in the same token
+// order, so the same bits), streamed: each thread copies its next rows of 16 bytes into shared
+// memory with cp.async while it sums earlier ones, so a thread always has loads in flight
+// instead of alternating between loading and summing.  The staging area is
 // [stage][row][thread] (16-byte words), so the 32 lanes of a warp touch consecutive words.
+// bf16 keys sum by TwoSum (blocks of at most 64 tokens), f16 keys by the int64 path.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -255,13 +256,18 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-constexpr int kStreamThreads = 256;
-constexpr int kStreamStages = 3;
-constexpr int kStreamSmem = kStreamStages * 8 * kStreamThreads * 16;  // 96 KB
+// Two shapes: large problems keep three chunks of 8 rows in flight per thread (256 threads,
+// 96 KB, two CTAs per SM); small ones (a few CTAs) put a whole 64-row block in flight at once
+// (64 threads, 64 KB) so the pass costs one memory round trip instead of eight.
+template <int kThreads, int kStages>
+struct StreamShape {
+    static constexpr int kSmem = kStages * 8 * kThreads * 16;
+};
 
-__global__ void __launch_bounds__(kStreamThreads, 2)
-centroid_partial_bf16_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S, int64_t D,
-                             int64_t block, int64_t nb, int spread_limit, double *__restrict__ part) {
+template <int kThreads, int kStages, bool kBF16>
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? 2 : 1)
+centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S, int64_t D, int64_t block,
+                        int64_t nb, int spread_limit, double *__restrict__ part) {
     extern __shared__ __align__(16) uint4 stage[];
     const uint32_t stage0 = smem_u32(stage) + threadIdx.x * 16u;
     const int64_t groups = D / 8;
@@ -274,77 +280,97 @@ centroid_partial_bf16_stream(const uint16_t *__restrict__ K, int64_t lanes, int6
         const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
         const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
         double *dst = part + lb * D + g * 8;
+        // bf16 state: hi + lo pairs and packed |bits| max/min; f16 state: int64 column sums
         uint64_t hi[4], lo[4];
         uint32_t mx[4], mn[4];
+        ColumnSum cs[kBF16 ? 1 : 8];
+        if constexpr (kBF16) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            hi[i] = f2_pack(0.f, 0.f);
-            lo[i] = hi[i];
-            mx[i] = 0u;
-            mn[i] = 0xFFFFFFFFu;
+            for (int i = 0; i < 4; ++i) {
+                hi[i] = f2_pack(0.f, 0.f);
+                lo[i] = hi[i];
+                mx[i] = 0u;
+                mn[i] = 0xFFFFFFFFu;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) col_init(cs[i]);
         }
-        auto two_sum = [&](int i, uint32_t x) {
-            const uint64_t v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-            const uint64_t s = f2_add(hi[i], v);
-            const uint64_t bv = f2_sub(s, hi[i]);
-            const uint64_t err = f2_add(f2_sub(hi[i], f2_sub(s, bv)), f2_sub(v, bv));
-            lo[i] = f2_add(lo[i], err);
-            hi[i] = s;
-            const uint32_t a = x & 0x7FFF7FFFu;
-            mx[i] = __vmaxu2(mx[i], a);
-            mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
+        auto add_word = [&](int i, uint32_t x) {
+            if constexpr (kBF16) {
+                // hi + lo += x exactly (TwoSum), two columns per packed operation
+                const uint64_t v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+                const uint64_t s = f2_add(hi[i], v);
+                const uint64_t bv = f2_sub(s, hi[i]);
+                const uint64_t err = f2_add(f2_sub(hi[i], f2_sub(s, bv)), f2_sub(v, bv));
+                lo[i] = f2_add(lo[i], err);
+                hi[i] = s;
+                const uint32_t a = x & 0x7FFF7FFFu;
+                mx[i] = __vmaxu2(mx[i], a);
+                mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
+            } else {
+                col_add(cs[2 * i], x & 0xFFFFu, false);
+                col_add(cs[2 * i + 1], x >> 16, false);
+            }
+        };
+        auto add_row = [&](const uint4 v) {
+            add_word(0, v.x);
+            add_word(1, v.y);
+            add_word(2, v.z);
+            add_word(3, v.w);
         };
         const int64_t chunks = n >> 3;  // whole chunks of 8 tokens
         const int64_t full = chunks << 3;
-        // Ring of kStreamStages chunks; one commit group per chunk slot (empty past the end), so
-        // wait_group<kStreamStages - 1> always means "chunk c has landed".
+        // Ring of kStages chunks; one commit group per chunk slot (empty past the end), so
+        // wait_group<kStages - 1> always means "chunk c has landed".
         auto issue = [&](int64_t c) {
             if (c < chunks) {
-                const int buf = (int)(c % kStreamStages);
+                const int buf = (int)(c % kStages);
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    cp_async16(stage0 + (uint32_t)((buf * 8 + u) * kStreamThreads * 16), src + (c * 8 + u) * D);
+                    cp_async16(stage0 + (uint32_t)((buf * 8 + u) * kThreads * 16), src + (c * 8 + u) * D);
             }
             cp_async_commit();
         };
 #pragma unroll
-        for (int c = 0; c < kStreamStages - 1; ++c) issue(c);
+        for (int c = 0; c < kStages - 1; ++c) issue(c);
         for (int64_t c = 0; c < chunks; ++c) {
-            issue(c + kStreamStages - 1);
-            cp_async_wait<kStreamStages - 1>();
-            const int buf = (int)(c % kStreamStages);
+            issue(c + kStages - 1);
+            cp_async_wait<kStages - 1>();
+            const int buf = (int)(c % kStages);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint4 v = stage[(buf * 8 + u) * kStreamThreads + threadIdx.x];
-                two_sum(0, v.x);
-                two_sum(1, v.y);
-                two_sum(2, v.z);
-                two_sum(3, v.w);
-            }
+            for (int u = 0; u < 8; ++u) add_row(stage[(buf * 8 + u) * kThreads + threadIdx.x]);
         }
         cp_async_wait<0>();
-        for (int64_t t = full; t < n; ++t) {
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
-            two_sum(0, v.x);
-            two_sum(1, v.y);
-            two_sum(2, v.z);
-            two_sum(3, v.w);
-        }
+        for (int64_t t = full; t < n; ++t) add_row(__ldg(reinterpret_cast<const uint4 *>(src + t * D)));
+        if constexpr (kBF16) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            float h0, h1, l0, l1;
-            f2_unpack(hi[i], h0, h1);
-            f2_unpack(lo[i], l0, l1);
+            for (int i = 0; i < 4; ++i) {
+                float h0, h1, l0, l1;
+                f2_unpack(hi[i], h0, h1);
+                f2_unpack(lo[i], l0, l1);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
-                const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
-                const int emax = (int)(amax >> 7);
-                const int emin = max(1, (int)(amin >> 7));
-                const bool all_zero = amin == 0xFFFFu;
-                const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
-                dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
-                                       : column_sum_exact_slow(src + 2 * i + h, D, n, true, spread_limit);
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
+                    const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
+                    const int emax = (int)(amax >> 7);
+                    const int emin = max(1, (int)(amin >> 7));
+                    const bool all_zero = amin == 0xFFFFu;
+                    const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
+                    dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
+                                           : column_sum_exact_slow(src + 2 * i + h, D, n, true, spread_limit);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (col_exact(cs[i], false, n, spread_limit)) {
+                    dst[i] = col_value(cs[i], false);
+                } else {
+                    double acc = 0.0;
+                    for (int64_t tt = 0; tt < n; ++tt) acc += widen(__ldg(src + tt * D + i), false);
+                    dst[i] = acc;
+                }
             }
         }
     }
@@ -377,6 +403,13 @@ __global__ void centroid_partial_scalar(const uint16_t *__restrict__ K, bool bf1
 
 // C[b][d] = (sum_{l ascending} part[l][b][d]) / (n_b * lanes), n_b the tokens block b holds
 // (block, or fewer for a partial last block).
+// Pins eight loaded values in registers at this point: the loads that produced them are
+// issued before it and the arithmetic that uses them comes after, so independent loads are in
+// flight together instead of being interleaved with a dependent add chain.
+__device__ __forceinline__ void hold8(double *v) {
+    asm volatile("" : "+d"(v[0]), "+d"(v[1]), "+d"(v[2]), "+d"(v[3]), "+d"(v[4]), "+d"(v[5]), "+d"(v[6]), "+d"(v[7]));
+}
+
 __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, int64_t nb,
                                int64_t D, int64_t S, int64_t block, double *__restrict__ C) {
     const int64_t n = nb * D;
@@ -384,8 +417,19 @@ __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, i
          w += (int64_t)gridDim.x * blockDim.x) {
         const int64_t b = w / D;
         const int64_t n_b = (b + 1) * block <= S ? block : S - b * block;
+        // lanes in ascending order; the loads of 16 lanes are issued before their adds
         double total = 0.0;
-        for (int64_t l = 0; l < lanes; ++l) total += part[l * n + w];
+        int64_t l = 0;
+        for (; l + 16 <= lanes; l += 16) {
+            double v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = __ldg(part + (l + i) * n + w);
+            hold8(v);
+            hold8(v + 8);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) total += v[i];
+        }
+        for (; l < lanes; ++l) total += part[l * n + w];
         C[w] = total / (double)(n_b * lanes);
     }
 }
@@ -443,6 +487,7 @@ __global__ void permute_rows(const double *__restrict__ C, const int *__restrict
 // ---------------------------------------------------------------- pairwise distances
 constexpr int kPdTile = 16;   // pairs per tile side
 constexpr int kPdChunk = 32;  // d values staged per step
+constexpr int kPdFlatBelow = 256;  // nb below which pairwise_d2_flat runs instead
 
 // D2[u][v] = D2[v][u] = sum_{d ascending} fma(C[u][d]-C[v][d], same, acc).  One CTA per tile
 // (tu <= tv) of the upper triangle, 64 threads, 2 x 2 pairs each.  (C[v]-C[u] is exactly
@@ -491,6 +536,55 @@ __global__ void __launch_bounds__(64) pairwise_d2(const double *__restrict__ C, 
         }
 }
 
+// The same distances for small nb, where the tiled kernel would run a handful of CTAs (one
+// at nb = 16): one thread per pair u < v, 32 pairs per CTA, so the FP64 chains spread over
+// as many SMs as there are warps.  The diagonal is written as +0, like the tiled kernel's
+// fma(0, 0, 0).
+__global__ void __launch_bounds__(32) pairwise_d2_flat(const double *__restrict__ C, int64_t nb, int64_t D,
+                                                       double *__restrict__ D2) {
+    const int64_t npairs = nb * (nb - 1) / 2;
+    const int64_t p = (int64_t)blockIdx.x * 32 + threadIdx.x;
+    if (p < nb) D2[p * nb + p] = 0.0;
+    if (p >= npairs) return;
+    // p -> (u, v), u < v, row-major over the strict upper triangle: row u starts at
+    // u * (2 nb - u - 1) / 2.  Float estimate, then exact integer correction.
+    const double fnb = (double)nb;
+    int64_t u = (int64_t)floor(((2.0 * fnb - 1.0) - sqrt((2.0 * fnb - 1.0) * (2.0 * fnb - 1.0) - 8.0 * (double)p)) / 2.0);
+    if (u < 0) u = 0;
+    if (u > nb - 2) u = nb - 2;
+    while (u > 0 && u * (2 * nb - u - 1) / 2 > p) --u;
+    while ((u + 1) * (2 * nb - u - 2) / 2 <= p) ++u;
+    const int64_t v = u + 1 + (p - u * (2 * nb - u - 1) / 2);
+    const double *cu = C + u * D, *cv = C + v * D;
+    // d ascending; the loads of 32 d are issued before their fma chain
+    double acc = 0.0;
+    int64_t d = 0;
+    for (; d + 32 <= D; d += 32) {
+        double a[32], b[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            a[i] = __ldg(cu + d + i);
+            b[i] = __ldg(cv + d + i);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+            hold8(a + i);
+            hold8(b + i);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const double t = a[i] - b[i];
+            acc = fma(t, t, acc);
+        }
+    }
+    for (; d < D; ++d) {
+        const double t = __ldg(cu + d) - __ldg(cv + d);
+        acc = fma(t, t, acc);
+    }
+    D2[u * nb + v] = acc;
+    D2[v * nb + u] = acc;
+}
+
 // ---------------------------------------------------------------- MST, elder rule, CSR
 // One cooperative launch runs everything after the distance matrix.  Its CTAs are all
 // resident (cudaLaunchCooperativeKernel), so they can meet at grid-wide barriers; the barrier
@@ -516,7 +610,7 @@ struct GraphArgs {
     double *mst_d;
     int *mst_u, *mst_v;
     int *counters;   // [0] components, [1] MST edges recorded, [2] CSR overflow
-    unsigned *gbar;  // [0] arrivals, [1] generation, [2] gave up
+    unsigned *gbar;  // [0] arrivals so far, [2] a CTA gave up waiting
     double *sal;
     const int *perm; // content rule: block of each rank (the graph runs on ranks); else null
     double *sal_rank; // content rule: salience by rank, before the scatter to blocks
@@ -531,30 +625,29 @@ struct GraphArgs {
 __device__ bool grid_sync(unsigned *gbar, const DeviceFlags &f) {
     __shared__ int s_ok;
     __syncthreads();
+    // A lone CTA needs nothing more: __syncthreads orders its threads' global accesses.
+    if (gridDim.x == 1) return true;
     if (threadIdx.x == 0) {
-        volatile unsigned *vg = gbar;
-        int ok = vg[2] == 0u;
-        if (ok) {
-            const unsigned gen = vg[1];
-            __threadfence();
-            if (atomicAdd(&gbar[0], 1u) == gridDim.x - 1) {
-                atomicExch(&gbar[0], 0u);
-                __threadfence();
-                atomicAdd(&gbar[1], 1u);
-            } else {
-                const unsigned long long t0 = globaltimer();
-                while (vg[1] == gen) {
-                    if (vg[2] != 0u) { ok = 0; break; }
-                    if (globaltimer() - t0 > kWaitTimeoutNs) {
-                        atomicExch(&gbar[2], 1u);
-                        raise_status(f, kDevTimeout);
-                        ok = 0;
-                        break;
-                    }
+        // gbar[0] counts arrivals over the whole launch (zeroed before it), so barrier k is
+        // passed once the count reaches (k + 1) * gridDim.x: one atomic per CTA and no reset.
+        int ok = 1;
+        __threadfence();
+        const unsigned arrived = atomicAdd(&gbar[0], 1u) + 1u;
+        const unsigned target = (arrived + gridDim.x - 1u) / gridDim.x * gridDim.x;
+        if (arrived != target) {
+            volatile unsigned *vg = gbar;
+            const unsigned long long t0 = globaltimer();
+            while (vg[0] < target) {
+                if (vg[2] != 0u) { ok = 0; break; }
+                if (globaltimer() - t0 > kWaitTimeoutNs) {
+                    atomicExch(&gbar[2], 1u);
+                    raise_status(f, kDevTimeout);
+                    ok = 0;
+                    break;
                 }
             }
-            __threadfence();
         }
+        __threadfence();
         s_ok = ok;
     }
     __syncthreads();
@@ -706,10 +799,13 @@ __device__ void bitonic_sort_pairs(unsigned long long *k1, unsigned long long *k
 // Bitonic sort of (k1, k2) pairs ascending with one element per thread (n == blockDim.x, a
 // power of two): strides below 32 exchange through shuffles, larger ones through `xs`
 // (2 * n words of shared memory).  On return k1/k2 hold the element of rank threadIdx.x.
+// Sorts the keys of threads [0, m) (m a power of two, m <= blockDim.x) ascending; threads at
+// or past m exchange only among themselves (i ^ stride >= m there), so their keys are left in
+// some order of their own.  Every thread must call it (the cross-warp stages synchronize).
 __device__ void bitonic_sort_regs(unsigned long long &k1, unsigned long long &k2,
-                                  unsigned long long *xs) {
+                                  unsigned long long *xs, int m) {
     const int i = threadIdx.x, n = blockDim.x;
-    for (int size = 2; size <= n; size <<= 1) {
+    for (int size = 2; size <= m; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
             unsigned long long p1, p2;
             if (stride < 32) {
@@ -768,7 +864,7 @@ __device__ void elder_phase(const GraphArgs &a, uint8_t *sm, int n_edges, unsign
         unsigned long long k1 = threadIdx.x < pow2 ? kd[threadIdx.x] : ~0ull;
         unsigned long long k2 = threadIdx.x < pow2 ? kab[threadIdx.x] : ~0ull;
         __syncthreads();
-        bitonic_sort_regs(k1, k2, xs);
+        bitonic_sort_regs(k1, k2, xs, pow2);
         __syncthreads();
         if (threadIdx.x < pow2) {
             kd[threadIdx.x] = k1;
@@ -955,7 +1051,7 @@ __global__ void __launch_bounds__(512) schedule_graph_kernel(GraphArgs a) {
         unsigned long long k1 = tid < pow2 ? ok1[tid] : ~0ull;
         unsigned long long k2 = tid < pow2 ? ok2[tid] : ~0ull;
         __syncthreads();
-        bitonic_sort_regs(k1, k2, xs);
+        bitonic_sort_regs(k1, k2, xs, pow2);
         if (tid < nb) order[tid] = (int)k2;
     } else {
         bitonic_sort_pairs(ok1, ok2, pow2);
@@ -1108,12 +1204,18 @@ tsa_status launch_block_sums(const ScheduleLaunch &a, double *part) {
     int log2_block = 0;
     while ((int64_t(1) << log2_block) < a.block) ++log2_block;
     const int spread_limit = 45 - log2_block;
-    if (vec && a.bf16) {
-        if (cudaFuncSetAttribute(centroid_partial_bf16_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kStreamSmem) != cudaSuccess)
+    if (vec && (!a.bf16 || a.block <= 64)) {  // the TwoSum exactness bound holds for <= 64 terms
+        // the small shape only while it fills at most one CTA per SM
+        const bool large = items >= (int64_t)152 * 64;
+        auto kern = large ? (a.bf16 ? centroid_partial_stream<256, 3, true> : centroid_partial_stream<256, 3, false>)
+                          : (a.bf16 ? centroid_partial_stream<64, 8, true> : centroid_partial_stream<64, 8, false>);
+        const int nthr = large ? 256 : 64;
+        const int smem = large ? StreamShape<256, 3>::kSmem : StreamShape<64, 8>::kSmem;
+        const int64_t nblk = (items + nthr - 1) / nthr;
+        const unsigned sgrid = (unsigned)(nblk < 152 * 64 ? nblk : 152 * 64);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return TSA_ERR_CUDA;
-        centroid_partial_bf16_stream<<<grid, kStreamThreads, kStreamSmem, st>>>(a.K, a.lanes, a.S, a.D, a.block,
-                                                                                a.nb, spread_limit, part);
+        kern<<<sgrid, nthr, smem, st>>>(a.K, a.lanes, a.S, a.D, a.block, a.nb, spread_limit, part);
     } else if (vec)
         centroid_partial_vec8<<<grid, threads, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
                                                         spread_limit, part);
@@ -1169,7 +1271,11 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
         graph_cent = part;  // the workspace's block-sum area; centroid_final has read the sums
     }
     // distances
-    {
+    if (nb < kPdFlatBelow) {
+        const int64_t npairs = a.nb * (a.nb - 1) / 2;
+        const int64_t n = npairs > a.nb ? npairs : a.nb;
+        pairwise_d2_flat<<<(unsigned)((n + 31) / 32), 32, 0, st>>>(graph_cent, a.nb, a.D, d2);
+    } else {
         const int t = (nb + kPdTile - 1) / kPdTile;
         pairwise_d2<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(graph_cent, a.nb, a.D, t, d2);
     }
