@@ -640,8 +640,8 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             o_valid = mbar_wait(bar_o_done, (u - 1) & 1, flags);
             if (!o_valid) *abort_flag = 1;
         }
-        named_barrier(1, kRows);
-        if (*abort_flag == 0) {
+        // one decision for all softmax warps (the section below has a barrier of its own)
+        if (!named_barrier_or(1, kRows, *abort_flag != 0)) {
             tc_fence_after();
             const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
             // A partial last query block (S not a multiple of 64) is not TMA-stored -- its box

@@ -588,8 +588,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             acc_valid = mbar_wait(bar_done, (u - 1) & 1, flags);
             if (!acc_valid) *abort_flag = 1;
         }
-        named_barrier(1, kRows);
-        if (*abort_flag == 0) {
+        // one decision for all elementwise warps (the section below has a barrier of its own)
+        if (!named_barrier_or(1, kRows, *abort_flag != 0)) {
             tc_fence_after();
             __syncwarp();
             // every product that read Q has completed: Q's tile stages dQ
@@ -898,8 +898,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             acc_valid = mbar_wait(bar_done, (u - 1) & 1, flags);
             if (!acc_valid) *abort_flag = 1;
         }
-        named_barrier(1, kRows);
-        if (*abort_flag == 0) {
+        // one decision for all elementwise warps (the section below has a barrier of its own)
+        if (!named_barrier_or(1, kRows, *abort_flag != 0)) {
             tc_fence_after();
             __syncwarp();
             // every product that read K and V has completed: their tiles stage dK and dV
