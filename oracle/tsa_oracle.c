@@ -767,7 +767,9 @@ int oracle_attention_backward(const uint16_t *Q, const uint16_t *K, const uint16
                               const int32_t *col_idx, double *dQ, double *dK, double *dV,
                               int nthreads)
 {
-    if (block <= 0 || S % block != 0 || L <= 0 || D <= 0) return 1;
+    /* S need not be a multiple of block: row i = q / block of a query q < S only reaches
+     * keys k <= q < S, so a partial last block needs nothing else. */
+    if (block <= 0 || S <= 0 || L <= 0 || D <= 0) return 1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     if (nthreads > L) nthreads = (int)L;

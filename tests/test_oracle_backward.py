@@ -9,7 +9,9 @@ What pins what:
   gradients sum to the upstream gradient of the rows that have keys; a query with a single
   allowed key has an exactly zero query gradient;
 * log-sum-exp -- scipy.special.logsumexp over the same masked scores, -inf for rows without
-  keys, and scale * <q, k> for single-key rows.
+  keys, and scale * <q, k> for single-key rows;
+* a sequence whose length is not a multiple of the block (a partial last block): the same
+  autograd comparison with the mask cut at S.
 """
 import numpy as np
 import pytest
@@ -20,7 +22,7 @@ import oracle
 
 
 def _mask(row_ptr, col_idx, S, block):
-    nb = S // block
+    nb = -(-S // block)  # a partial last block counts
     M = np.zeros((S, S), dtype=bool)
     for i in range(nb):
         for j in col_idx[row_ptr[i]:row_ptr[i + 1]]:
@@ -97,3 +99,26 @@ def test_lse_matches_logsumexp():
         single = M.sum(axis=1) == 1  # one allowed key: lse is that key's scaled score
         only = np.where(M[None], s, -np.inf).max(axis=-1)
         assert np.abs(lse[:, single] - only[:, single]).max() <= 1e-12, kind
+
+
+@pytest.mark.parametrize("S", [163, 129, 31])
+@pytest.mark.parametrize("kind", ["dense", "random"])
+def test_partial_last_block_gradients_equal_autograd(S, kind):
+    g = torch.Generator().manual_seed(S)
+    L, D, block, scale = 2, 16, 32, 0.3
+    Q, K, V, dO = (torch.randn((L, S, D), generator=g).to(torch.bfloat16) for _ in range(4))
+    nb = -(-S // block)
+    if kind == "dense":
+        rp, ci = oracle.dense_causal_csr(nb)
+    else:
+        rng = np.random.default_rng(S)
+        rows = [sorted(set(rng.choice(i + 1, size=rng.integers(1, i + 2), replace=False).tolist()) | {i})
+                for i in range(nb)]
+        rp = np.zeros(nb + 1, np.int32)
+        rp[1:] = np.cumsum([len(r) for r in rows])
+        ci = np.array([j for r in rows for j in r], np.int32)
+    dq, dk, dv = oracle.attention_backward(Q, K, V, dO, rp, ci, block, scale, nthreads=2)
+    rq, rk, rv, _ = _autograd(Q, K, V, dO, _mask(rp, ci, S, block), scale)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert got.shape == (L, S, D)
+        assert np.abs(got - ref).max() <= 1e-10 * max(1.0, np.abs(ref).max())
