@@ -5,7 +5,8 @@ block's centroid averages the tokens it holds).  Attention: element by element a
 oracle within the tolerance of test_gpu_attention (2e-3 fp16, 1e-2 bf16, one output ulp where
 the format is coarser), every lane compared, so a partial block that wrote past its lane's last
 row into the next lane would show; rows past the last lane's end and log-sum-exp entries past
-the end stay untouched.  The backward pass needs whole blocks and says so.
+the end stay untouched.  Backward: dQ, dK, dV against the oracle within test_gpu_backward's
+tolerance, with the same untouched-tail check.
 """
 import numpy as np
 import pytest
@@ -14,6 +15,7 @@ import torch
 import oracle
 import topology_scheduled_gb300 as tsa
 from test_gpu_attention import assert_close
+from test_gpu_backward import U, _close, _schedule
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -81,9 +83,29 @@ def test_attention_matches_oracle(L, S, D, dtype, kind):
     assert np.abs(lse.double().numpy() - ref_lse).max() <= u
 
 
-def test_backward_needs_whole_blocks():
-    x = torch.zeros((1, 100, 64), dtype=torch.float16, device=DEV)
-    lse = torch.zeros((1, 100), dtype=torch.float32, device=DEV)
-    rp, ci = tsa.tsa_dense_causal_csr(100, 64)
-    with pytest.raises(tsa.TsaError):
-        tsa.tsa_scheduled_attention_backward(x, x, x, x, x, lse, rp, ci, 0.125)
+@pytest.mark.parametrize("L,S,D,dtype,kind", [(1, 100, 64, torch.float16, "dense"),
+                                                (3, 1000, 128, torch.bfloat16, "random"),
+                                                (2, 4133, 64, torch.bfloat16, "holes"),
+                                                (2, 130, 128, torch.float16, "dense"),
+                                                (1, 8191, 128, torch.bfloat16, "random")])
+def test_backward_matches_oracle(L, S, D, dtype, kind):
+    """dQ, dK, dV with a partial last block, every lane against the oracle; rows past the last
+    lane's end stay untouched (a partial block is stored row by row, not as a 64-row box)."""
+    q, k, v = _qkv(L, S, D, dtype, 3 * S + D)
+    g = torch.Generator().manual_seed(S)
+    dO = torch.randn((L, S, D), generator=g).to(dtype)
+    nb = -(-S // 64)
+    rp, ci = _schedule(kind, nb, seed=L)
+    scale = D ** -0.5
+    rpd, cid = torch.as_tensor(rp, device=DEV), torch.as_tensor(ci, device=DEV)
+    O, lse = tsa.tsa_scheduled_attention_fwd(q.to(DEV), k.to(DEV), v.to(DEV), rpd, cid, scale)
+    bufs = [torch.full((L * S + 64, D), 7.0, dtype=dtype, device=DEV) for _ in range(3)]
+    grads = [b[: L * S].view(L, S, D) for b in bufs]
+    tsa.tsa_scheduled_attention_backward(q.to(DEV), k.to(DEV), v.to(DEV), O, dO.to(DEV), lse, rpd, cid,
+                                         scale, dq=grads[0], dk=grads[1], dv=grads[2])
+    assert tsa.tsa_last_device_status() == 0
+    for b in bufs:
+        assert bool((b[L * S:] == 7.0).all())
+    refs = oracle.attention_backward(q, k, v, dO, rp, ci, 64, scale, nthreads=8)
+    for name, got, ref in zip(("dQ", "dK", "dV"), grads, refs):
+        _close(got, ref, U[dtype], f"{kind} {name}")

@@ -423,8 +423,8 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
 }
 
 size_t tsa_attention_backward_workspace_bytes(int64_t lanes, int64_t S, int64_t block, int64_t nnz_cap) {
-    if (lanes <= 0 || S <= 0 || block != 64 || S % block != 0 || nnz_cap < 1) return 0;
-    const int64_t nb = S / block;
+    if (lanes <= 0 || S <= 0 || block != 64 || nnz_cap < 1) return 0;
+    const int64_t nb = (S + block - 1) / block;  // a partial last block counts
     if (nb > kMaxBackwardBlocks || lanes * S >= (int64_t)INT_MAX) return 0;
     return backward_workspace_layout(lanes, S, nb, nnz_cap).total;
 }
@@ -441,9 +441,8 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0 || nnz_cap < 1) return TSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
     if (block != 64 || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
-    if (S % block != 0) return TSA_ERR_UNSUPPORTED;  // the backward pass needs whole blocks
     if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
-    const int64_t lanes = B * H, nb = S / block;
+    const int64_t lanes = B * H, nb = (S + block - 1) / block;  // a partial last block counts
     if (lanes * S >= (int64_t)INT_MAX || nb > kMaxBackwardBlocks) return TSA_ERR_UNSUPPORTED;
     const void *ins[] = {Q, K, V, O, dO};
     void *outs[] = {dQ, dK, dV};
@@ -492,11 +491,15 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     a.tmdV64 = &tdV64;
     a.O = static_cast<const uint16_t *>(O);
     a.dO = static_cast<const uint16_t *>(dO);
+    a.dQ = static_cast<uint16_t *>(dQ);
+    a.dK = static_cast<uint16_t *>(dK);
+    a.dV = static_cast<uint16_t *>(dV);
     a.lse = lse;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;
     a.nnz_cap = nnz_cap;
     a.delta = reinterpret_cast<float *>(w + ws.delta);
+    a.lse_pad = reinterpret_cast<float *>(w + ws.lse_pad);
     a.vlen = reinterpret_cast<int *>(w + ws.vlen);
     a.cnt = reinterpret_cast<int *>(w + ws.cnt);
     a.col_ptr = reinterpret_cast<int *>(w + ws.col_ptr);

@@ -205,17 +205,24 @@ __device__ __forceinline__ float to_f32(uint32_t h16) {
 }
 
 // D/8 threads per row, 16-byte loads, fp32 products summed in the thread then across the group.
+// Rows are laid out per lane over Sp = nb * 64 tokens; the tokens past S (a partial last block)
+// get Delta 0 and log-sum-exp -inf, and the given log-sum-exp is copied into the same layout.
 template <bool kBF16>
-__global__ void bwd_delta(const uint16_t *__restrict__ O, const uint16_t *__restrict__ dO, long long rows,
-                          int D, float *__restrict__ delta) {
+__global__ void bwd_delta(const uint16_t *__restrict__ O, const uint16_t *__restrict__ dO,
+                          const float *__restrict__ lse, long long lanes, int S, int Sp, int D,
+                          float *__restrict__ delta, float *__restrict__ lse_pad) {
     const int g = D >> 3;  // 8 or 16 lanes per row, so a row never straddles a warp
-    const long long total = rows * g;
+    const long long total = lanes * Sp * g;
     const long long stride = (long long)gridDim.x * blockDim.x;
     for (long long base = (long long)blockIdx.x * blockDim.x; base < total; base += stride) {
         const long long x = base + threadIdx.x;
         float acc = 0.f;
-        if (x < total) {
-            const long long r = x / g;
+        const long long pr = x / g;          // padded row
+        const long long l = pr / Sp;
+        const int t = (int)(pr % Sp);        // token within the lane
+        const bool real = x < total && t < S;
+        const long long r = l * S + t;       // row of O, dO and lse
+        if (real) {
             const int c = (int)(x % g);
             const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + r * D + c * 8));
             const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + r * D + c * 8));
@@ -227,7 +234,10 @@ __global__ void bwd_delta(const uint16_t *__restrict__ O, const uint16_t *__rest
             }
         }
         for (int off = g >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (x < total && (x % g) == 0) delta[x / g] = acc;
+        if (x < total && (x % g) == 0) {
+            delta[pr] = acc;
+            lse_pad[pr] = real ? __ldg(lse + r) : -INFINITY;
+        }
     }
 }
 
@@ -297,6 +307,22 @@ __device__ __forceinline__ void stage_rows(uint32_t tmem_row, uint32_t col, bool
     }
 }
 
+// Row `row` (0-127) of a 128-row SW128 staging tile (the layout stage_rows writes: 64-column
+// chunks of 16 KB, 16-byte units of a row permuted by row & 7) copied to a global row of D
+// 16-bit values.
+template <int D>
+__device__ __forceinline__ void copy_staged_row(const uint8_t *tile, int row, uint16_t *dst) {
+    const uint32_t sw = (uint32_t)(row & 7);
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) {
+        const uint8_t *src = tile + c * 16384 + row * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            *reinterpret_cast<uint4 *>(dst + c * 64 + u * 8) =
+                *reinterpret_cast<const uint4 *>(src + (((uint32_t)u ^ sw) << 4));
+    }
+}
+
 // Meta area (byte offsets from the meta base), common to both kernels.
 constexpr int kBarTile = 0;        // resident tile(s) loaded
 constexpr int kBarFull = 8;        // kStream x 8: streamed block landed
@@ -343,7 +369,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               const __grid_constant__ CUtensorMap tmdQ, const int32_t *__restrict__ row_ptr,
               const int32_t *__restrict__ col_idx, const int *__restrict__ vlen,
               const float *__restrict__ lse, const float *__restrict__ delta, int nb, int S,
-              float scale, float scale_log2, DeviceFlags flags) {
+              float scale, float scale_log2, uint16_t *__restrict__ dQ, DeviceFlags flags) {
     using L = DqSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (__syncthreads_or(threadIdx.x == 0 &&
@@ -538,7 +564,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const int my_block = qa + half;
         const bool row_exists = half == 0 || has_b;
         const uint32_t t_lane = (uint32_t)(warp * 32) << 16;
-        const long long grow = (long long)row0 + (long long)qa * kBlock + tid;
+        // the row in the per-lane padded Delta / log-sum-exp arrays (nb * 64 rows per lane)
+        const long long grow = ((long long)lane_id * nb + qa) * kBlock + tid;
         const float lse2 = row_exists ? lse[grow] * kLog2e : -INFINITY;
         const float dlt = row_exists ? delta[grow] : 0.f;
         const bool live = lse2 > -INFINITY;  // a row with keys
@@ -596,15 +623,21 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             stage_rows<D, kBF16>(tmem + t_lane, kAccCol, acc_valid, scale, sQ, tid);
             fence_proxy_async_smem();
             named_barrier(1, kRows);
+            // A partial last block (S not a multiple of 64) is not TMA-stored -- its box would
+            // run into the next lane's rows -- but copied row by row from the staging tile.
+            const bool part_a = (qa + 1) * kBlock > S, part_b = has_b && (qa + 2) * kBlock > S;
             if (tid == 0) {
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_store_2d(&tmdQ, c * 64, row0 + qa * kBlock, sQ + c * 16384);
-                    if (has_b) tma_store_2d(&tmdQ, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
+                    if (!part_a) tma_store_2d(&tmdQ, c * 64, row0 + qa * kBlock, sQ + c * 16384);
+                    if (has_b && !part_b)
+                        tma_store_2d(&tmdQ, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
                 }
                 tma_store_commit();
                 tma_store_wait_all();
             }
+            if ((half ? part_b : part_a) && qa * kBlock + tid < S)
+                copy_staged_row<D>(smem + (sQ - base), tid, dQ + ((size_t)row0 + qa * kBlock + tid) * D);
         }
     }
 #undef BAR_K_FULL
@@ -649,7 +682,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                const int *__restrict__ col_ptr, const int32_t *__restrict__ row_idx,
                const int *__restrict__ pairs, const float *__restrict__ lse,
                const float *__restrict__ delta, int nb, int S, float scale, float scale_log2,
-               DeviceFlags flags) {
+               uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, DeviceFlags flags) {
     using L = DkvSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     if (__syncthreads_or(threadIdx.x == 0 &&
@@ -754,8 +787,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     tma_load_2d(sQ + s * L::kQBytes + c * 8192, &tmQ, c * 64, y, BAR_FULL(s));
                     tma_load_2d(sdO + s * L::kQBytes + c * 8192, &tmdO, c * 64, y, BAR_FULL(s));
                 }
-                bulk_load(sLse + s * 256, lse + y, 256, BAR_FULL(s));
-                bulk_load(sDelta + s * 256, delta + y, 256, BAR_FULL(s));
+                const long long py = ((long long)lane_id * nb + i) * kBlock;  // padded row
+                bulk_load(sLse + s * 256, lse + py, 256, BAR_FULL(s));
+                bulk_load(sDelta + s * 256, delta + py, 256, BAR_FULL(s));
                 issued = v + 1;
             }
             if (!ok) {
@@ -907,18 +941,27 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             stage_rows<D, kBF16>(tmem + t_lane, kDKCol, acc_valid, scale, sK, tid);
             fence_proxy_async_smem();
             named_barrier(1, kRows);
+            // a partial last key block is copied row by row (see the dQ kernel)
+            const bool part_a = (ka + 1) * kBlock > S, part_b = has_b && (kb + 1) * kBlock > S;
             if (tid == 0) {
 #pragma unroll
                 for (int c = 0; c < L::kChunks; ++c) {
-                    tma_store_2d(&tmdV, c * 64, row0 + ka * kBlock, sV + c * 16384);
-                    tma_store_2d(&tmdK, c * 64, row0 + ka * kBlock, sK + c * 16384);
-                    if (has_b) {
+                    if (!part_a) {
+                        tma_store_2d(&tmdV, c * 64, row0 + ka * kBlock, sV + c * 16384);
+                        tma_store_2d(&tmdK, c * 64, row0 + ka * kBlock, sK + c * 16384);
+                    }
+                    if (has_b && !part_b) {
                         tma_store_2d(&tmdV, c * 64, row0 + kb * kBlock, sV + c * 16384 + 8192);
                         tma_store_2d(&tmdK, c * 64, row0 + kb * kBlock, sK + c * 16384 + 8192);
                     }
                 }
                 tma_store_commit();
                 tma_store_wait_all();
+            }
+            if ((half ? part_b : part_a) && key_block * kBlock + k_in < S) {
+                const size_t grow_k = ((size_t)row0 + key_block * kBlock + k_in) * D;
+                copy_staged_row<D>(smem + (sV - base), tid, dV + grow_k);
+                copy_staged_row<D>(smem + (sK - base), tid, dK + grow_k);
             }
         }
     }
@@ -949,11 +992,11 @@ tsa_status launch_grad_kernels(const BwdLaunch &a) {
     const dim3 grid((unsigned)a.lanes, npairs);
     const float scale_log2 = a.scale * kLog2e;
     kq<<<grid, kThreads, DqSmem<D>::kBytes, a.stream>>>(*a.tmQ128, *a.tmdO128, *a.tmK64, *a.tmV64, *a.tmdQ64,
-                                                        a.row_ptr, a.col_idx, a.vlen, a.lse, a.delta, a.nb,
-                                                        a.S, a.scale, scale_log2, a.flags);
+                                                        a.row_ptr, a.col_idx, a.vlen, a.lse_pad, a.delta, a.nb,
+                                                        a.S, a.scale, scale_log2, a.dQ, a.flags);
     kkv<<<grid, kThreads, DkvSmem<D>::kBytes, a.stream>>>(*a.tmK64, *a.tmV64, *a.tmQ64, *a.tmdO64, *a.tmdK64,
-                                                          *a.tmdV64, a.col_ptr, a.row_idx, a.pairs, a.lse, a.delta,
-                                                          a.nb, a.S, a.scale, scale_log2, a.flags);
+                                                          *a.tmdV64, a.col_ptr, a.row_idx, a.pairs, a.lse_pad, a.delta,
+                                                          a.nb, a.S, a.scale, scale_log2, a.dK, a.dV, a.flags);
     return cudaGetLastError() == cudaSuccess ? TSA_OK : TSA_ERR_CUDA;
 }
 
@@ -968,7 +1011,8 @@ BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int
         return at;
     };
     const int64_t words = (nb + 31) / 32;
-    w.delta = take(sizeof(float) * (size_t)(lanes * S));
+    w.delta = take(sizeof(float) * (size_t)(lanes * nb * 64));  // rows padded to whole blocks
+    w.lse_pad = take(sizeof(float) * (size_t)(lanes * nb * 64));
     w.vlen = take(sizeof(int) * (size_t)nb);
     w.cnt = take(sizeof(int) * (size_t)nb);
     w.col_ptr = take(sizeof(int) * (size_t)(nb + 1));
@@ -999,13 +1043,14 @@ tsa_status launch_attention_backward(const BwdLaunch &a) {
         bwd_col_pairs<<<1, 1024, smem, st>>>(nb, pow2, a.cnt, a.pairs);
     }
     {
-        const long long items = (long long)a.lanes * a.S * (a.D / 8);
+        const int Sp = a.nb * kBlock;
+        const long long items = (long long)a.lanes * Sp * (a.D / 8);
         const long long blocks = (items + 255) / 256;
         const unsigned g = (unsigned)(blocks < 152 * 32 ? blocks : 152 * 32);
         if (a.bf16)
-            bwd_delta<true><<<g, 256, 0, st>>>(a.O, a.dO, (long long)a.lanes * a.S, a.D, a.delta);
+            bwd_delta<true><<<g, 256, 0, st>>>(a.O, a.dO, a.lse, a.lanes, a.S, Sp, a.D, a.delta, a.lse_pad);
         else
-            bwd_delta<false><<<g, 256, 0, st>>>(a.O, a.dO, (long long)a.lanes * a.S, a.D, a.delta);
+            bwd_delta<false><<<g, 256, 0, st>>>(a.O, a.dO, a.lse, a.lanes, a.S, Sp, a.D, a.delta, a.lse_pad);
     }
     if (cudaGetLastError() != cudaSuccess) return TSA_ERR_CUDA;
     if (a.D == 64) return a.bf16 ? launch_grad_kernels<64, true>(a) : launch_grad_kernels<64, false>(a);

@@ -36,7 +36,7 @@ tsa_status launch_scheduled_attention(const AttnLaunch &a);
 
 // Byte offsets of the backward pass's workspace regions (each 256-byte aligned).
 struct BwdWorkspace {
-    size_t delta, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, pairs, total;
+    size_t delta, lse_pad, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, pairs, total;
 };
 BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap);
 
@@ -48,10 +48,13 @@ struct BwdLaunch {
     const CUtensorMap *tmQ128, *tmdO128;
     const CUtensorMap *tmQ64, *tmdO64, *tmK64, *tmV64, *tmdQ64, *tmdK64, *tmdV64;
     const uint16_t *O, *dO;
+    uint16_t *dQ, *dK, *dV;  // for the row stores of a partial last block
     const float *lse;
     const int32_t *row_ptr, *col_idx;
     int64_t nnz_cap;
-    float *delta;
+    // Delta and the log-sum-exp per lane over nb * 64 rows (rows past S: 0 and -inf), so a
+    // partial last block is read like any other
+    float *delta, *lse_pad;
     int *vlen, *cnt, *col_ptr;
     unsigned *bitmap;
     size_t bitmap_bytes;
