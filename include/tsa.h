@@ -283,8 +283,11 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
  *                   256-byte aligned (Delta per row, the transposed schedule and its bitmap of
  *                   nb^2 bits); its contents on entry do not matter.
  *
- * Limits: block == 64, D in {64, 128}, nb = ceil(S/64) <= 8192 (a partial last block is
- * allowed: its rows are stored one by one, never past the lane's last row), B*H <= 65535,
+ * Limits: block in {64, 128} (a CSR of 128-token blocks is first expanded on the GPU into the
+ * 64-token CSR with the same allowed keys: rows 2p and 2p+1 hold 64-blocks 2j and 2j+1 of each
+ * j < p, plus 2p, and 2p+1 for row 2p+1, when p is in row p; a 32-token CSR is UNSUPPORTED),
+ * D in {64, 128}, ceil(S/64) <= 8192 (a partial last block is allowed: its rows are stored one
+ * by one, never past the lane's last row), B*H <= 65535,
  * B*H*S < 2^31.  Errors: INVALID_ARGUMENT, UNSUPPORTED, CAPACITY (workspace), NOT_DEVICE_POINTER,
  * DEVICE_MISMATCH, CUDA.  Device-side: BAD_SCHEDULE (a row is cut at its first bad entry, as in
  * the forward), TSA_ERR_DEVICE (nnz above nnz_cap: dK and dV then come out zero), TIMEOUT.

@@ -423,10 +423,12 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
 }
 
 size_t tsa_attention_backward_workspace_bytes(int64_t lanes, int64_t S, int64_t block, int64_t nnz_cap) {
-    if (lanes <= 0 || S <= 0 || block != 64 || nnz_cap < 1) return 0;
-    const int64_t nb = (S + block - 1) / block;  // a partial last block counts
-    if (nb > kMaxBackwardBlocks || lanes * S >= (int64_t)INT_MAX) return 0;
-    return backward_workspace_layout(lanes, S, nb, nnz_cap).total;
+    if (lanes <= 0 || S <= 0 || (block != 64 && block != 128) || nnz_cap < 1) return 0;
+    const int64_t nb = (S + 63) / 64;  // 64-token blocks; a partial last block counts
+    if (nb > kMaxBackwardBlocks || lanes * S >= (int64_t)INT_MAX || nnz_cap > INT_MAX / 4) return 0;
+    // a 128-token CSR is expanded to 64-token blocks first: up to 4 entries per entry
+    const int64_t nb_in = block == 128 ? (S + 127) / 128 : 0;
+    return backward_workspace_layout(lanes, S, nb, block == 128 ? 4 * nnz_cap : nnz_cap, nb_in).total;
 }
 
 tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const void *V, const void *O,
@@ -440,10 +442,14 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
     if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0 || nnz_cap < 1) return TSA_ERR_INVALID_ARGUMENT;
     if (!std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
-    if (block != 64 || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
+    if ((block != 64 && block != 128) || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
     if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
-    const int64_t lanes = B * H, nb = (S + block - 1) / block;  // a partial last block counts
-    if (lanes * S >= (int64_t)INT_MAX || nb > kMaxBackwardBlocks) return TSA_ERR_UNSUPPORTED;
+    // 64-token blocks (a partial last block counts); a 128-token CSR is expanded to them
+    const int64_t lanes = B * H, nb = (S + 63) / 64;
+    const int64_t nb_in = block == 128 ? (S + 127) / 128 : 0;
+    if (lanes * S >= (int64_t)INT_MAX || nb > kMaxBackwardBlocks || nnz_cap > INT_MAX / 4)
+        return TSA_ERR_UNSUPPORTED;
+    const int64_t cap = block == 128 ? 4 * nnz_cap : nnz_cap;
     const void *ins[] = {Q, K, V, O, dO};
     void *outs[] = {dQ, dK, dV};
     for (const void *p : ins)
@@ -460,7 +466,7 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
         for (int y = x + 1; y < 3; ++y)
             if (overlaps(outs[x], bytes, outs[y], bytes)) return TSA_ERR_INVALID_ARGUMENT;
     }
-    const BwdWorkspace ws = backward_workspace_layout(lanes, S, nb, nnz_cap);
+    const BwdWorkspace ws = backward_workspace_layout(lanes, S, nb, cap, nb_in);
     if (workspace_bytes < ws.total) return TSA_ERR_CAPACITY;
     int dev;
     TSA_TRY(current_device(&dev));
@@ -497,7 +503,11 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
     a.lse = lse;
     a.row_ptr = row_ptr;
     a.col_idx = col_idx;
-    a.nnz_cap = nnz_cap;
+    a.nnz_cap = cap;
+    a.nb_in = (int)nb_in;
+    a.vlen_in = reinterpret_cast<int *>(w + ws.vlen_in);
+    a.rp64 = reinterpret_cast<int32_t *>(w + ws.rp64);
+    a.ci64 = reinterpret_cast<int32_t *>(w + ws.ci64);
     a.delta = reinterpret_cast<float *>(w + ws.delta);
     a.lse_pad = reinterpret_cast<float *>(w + ws.lse_pad);
     a.vlen = reinterpret_cast<int *>(w + ws.vlen);

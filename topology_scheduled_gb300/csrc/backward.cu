@@ -81,6 +81,73 @@ __global__ void bwd_rows(int nb, const int32_t *__restrict__ row_ptr, const int3
     }
 }
 
+// A CSR of 128-token blocks as the CSR of 64-token blocks with the same allowed keys: query
+// block a = 2p + h (64 tokens) of 128-block row p holds the 64-blocks 2j and 2j+1 of every
+// j < p in row p, and of j = p the ones not after it (2p; 2p+1 when h = 1) -- the token mask
+// of the 64-token diagonal block then cuts keys k > q exactly as the 128-token rule does.
+// One warp per 128-block row: its valid prefix (the checks of bwd_rows), the two counts.
+__global__ void bwd_expand128_count(int nb128, int nb64, const int32_t *__restrict__ row_ptr,
+                                    const int32_t *__restrict__ col_idx, int *__restrict__ vlen128,
+                                    int *__restrict__ cnt64, DeviceFlags flags) {
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < nb128; p += nw) {
+        const int b = row_ptr[p], len = row_ptr[p + 1] - b;
+        int valid = 0;
+        if (len >= 0 && len <= p + 1) {
+            valid = len;
+            for (int e0 = 0; e0 < len; e0 += 32) {
+                const int e = e0 + lane;
+                bool bad = false;
+                if (e < len) {
+                    const int j = col_idx[b + e];
+                    const int prev = e > 0 ? col_idx[b + e - 1] : -1;
+                    bad = j < 0 || j > p || j <= prev;
+                }
+                const unsigned m = __ballot_sync(0xffffffffu, bad);
+                if (m) {
+                    valid = e0 + __ffs(m) - 1;
+                    break;
+                }
+            }
+        }
+        if (lane == 0) {
+            if (valid != len) raise_status(flags, kDevBadSchedule);
+            const int diag = valid > 0 && col_idx[b + valid - 1] == p ? 1 : 0;
+            const int below = valid - diag;
+            vlen128[p] = valid;
+            cnt64[2 * p] = 2 * below + diag;
+            if (2 * p + 1 < nb64) cnt64[2 * p + 1] = 2 * below + 2 * diag;
+        }
+    }
+}
+
+// One warp per 128-block row: writes the two 64-token rows at the scanned offsets.
+__global__ void bwd_expand128_fill(int nb128, int nb64, const int32_t *__restrict__ row_ptr,
+                                   const int32_t *__restrict__ col_idx, const int *__restrict__ vlen128,
+                                   const int *__restrict__ rp64, int32_t *__restrict__ ci64) {
+    const int lane = threadIdx.x & 31;
+    const int nw = gridDim.x * (blockDim.x >> 5);
+    for (int p = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < nb128; p += nw) {
+        const int b = row_ptr[p], valid = vlen128[p];
+        const bool second = 2 * p + 1 < nb64;
+        // an overflowing total leaves the offsets equal (every row empty): nothing to write
+        const int o0 = rp64[2 * p], o1 = second ? rp64[2 * p + 1] : 0;
+        const bool room0 = rp64[2 * p + 1] > o0 || valid == 0;
+        const bool room1 = second && (rp64[2 * p + 2] > o1 || valid == 0);
+        for (int e = lane; e < valid; e += 32) {
+            const int j = col_idx[b + e];
+            if (j < p) {
+                if (room0) { ci64[o0 + 2 * e] = 2 * j; ci64[o0 + 2 * e + 1] = 2 * j + 1; }
+                if (room1) { ci64[o1 + 2 * e] = 2 * j; ci64[o1 + 2 * e + 1] = 2 * j + 1; }
+            } else {  // j == p, the last entry
+                if (room0) ci64[o0 + 2 * e] = 2 * p;
+                if (room1) { ci64[o1 + 2 * e] = 2 * p; ci64[o1 + 2 * e + 1] = 2 * p + 1; }
+            }
+        }
+    }
+}
+
 // One warp per column: number of query blocks whose row holds it.
 __global__ void bwd_col_count(int nb, int words, const unsigned *__restrict__ bitmap, int *__restrict__ cnt) {
     const int lane = threadIdx.x & 31;
@@ -1002,7 +1069,7 @@ tsa_status launch_grad_kernels(const BwdLaunch &a) {
 
 }  // namespace
 
-BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap) {
+BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap, int64_t nb_in) {
     BwdWorkspace w{};
     size_t o = 0;
     auto take = [&](size_t bytes) {
@@ -1020,16 +1087,31 @@ BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int
     w.bitmap_bytes = sizeof(unsigned) * (size_t)(nb * words);
     w.row_idx = take(sizeof(int32_t) * (size_t)(nnz_cap > 0 ? nnz_cap : 1));
     w.pairs = take(sizeof(int) * (size_t)(2 * ((nb + 1) / 2)));
+    // a CSR of 128-token blocks (nb_in rows) expanded to 64-token blocks: nnz_cap is then the
+    // expanded capacity
+    w.vlen_in = take(sizeof(int) * (size_t)(nb_in > 0 ? nb_in : 1));
+    w.rp64 = take(sizeof(int32_t) * (size_t)(nb + 1));
+    w.ci64 = take(sizeof(int32_t) * (size_t)(nb_in > 0 ? nnz_cap : 1));
     w.total = o;
     return w;
 }
 
-tsa_status launch_attention_backward(const BwdLaunch &a) {
+tsa_status launch_attention_backward(const BwdLaunch &a_in) {
+    BwdLaunch a = a_in;
     cudaStream_t st = a.stream;
     const int nb = a.nb;
     const int words = (nb + 31) / 32;
-    if (cudaMemsetAsync(a.bitmap, 0, a.bitmap_bytes, st) != cudaSuccess) return TSA_ERR_CUDA;
     const unsigned wgrid = (unsigned)((nb + 7) / 8 < 152 * 8 ? (nb + 7) / 8 : 152 * 8);
+    if (a.nb_in > 0) {
+        // 128-token CSR: the equivalent 64-token CSR first (cnt is free until the columns)
+        const unsigned g = (unsigned)((a.nb_in + 7) / 8 < 152 * 8 ? (a.nb_in + 7) / 8 : 152 * 8);
+        bwd_expand128_count<<<g, 256, 0, st>>>(a.nb_in, nb, a.row_ptr, a.col_idx, a.vlen_in, a.cnt, a.flags);
+        bwd_col_scan<<<1, 1024, 0, st>>>(nb, a.cnt, a.rp64, (long long)a.nnz_cap, a.flags);
+        bwd_expand128_fill<<<g, 256, 0, st>>>(a.nb_in, nb, a.row_ptr, a.col_idx, a.vlen_in, a.rp64, a.ci64);
+        a.row_ptr = a.rp64;
+        a.col_idx = a.ci64;
+    }
+    if (cudaMemsetAsync(a.bitmap, 0, a.bitmap_bytes, st) != cudaSuccess) return TSA_ERR_CUDA;
     bwd_rows<<<wgrid, 256, 0, st>>>(nb, a.row_ptr, a.col_idx, words, a.vlen, a.bitmap, a.flags);
     bwd_col_count<<<wgrid, 256, 0, st>>>(nb, words, a.bitmap, a.cnt);
     bwd_col_scan<<<1, 1024, 0, st>>>(nb, a.cnt, a.col_ptr, (long long)a.nnz_cap, a.flags);

@@ -36,9 +36,10 @@ tsa_status launch_scheduled_attention(const AttnLaunch &a);
 
 // Byte offsets of the backward pass's workspace regions (each 256-byte aligned).
 struct BwdWorkspace {
-    size_t delta, lse_pad, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, pairs, total;
+    size_t delta, lse_pad, vlen, cnt, col_ptr, bitmap, bitmap_bytes, row_idx, pairs, vlen_in, rp64, ci64, total;
 };
-BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap);
+// nb: 64-token blocks; nb_in: rows of a 128-token CSR to expand first (0: the CSR is 64-token)
+BwdWorkspace backward_workspace_layout(int64_t lanes, int64_t S, int64_t nb, int64_t nnz_cap, int64_t nb_in);
 
 // Largest number of query blocks the backward pass accepts (its column bitmap is nb^2 bits).
 constexpr int64_t kMaxBackwardBlocks = 8192;
@@ -60,6 +61,9 @@ struct BwdLaunch {
     size_t bitmap_bytes;
     int32_t *row_idx;
     int *pairs;  // dK/dV key-block pairs, 2 per pair (-1: none)
+    int nb_in;   // > 0: row_ptr/col_idx are a CSR of nb_in 128-token blocks, expanded into
+    int *vlen_in;  // rp64/ci64 (64-token blocks, capacity nnz_cap) before anything else
+    int32_t *rp64, *ci64;
     int nb, S, D, lanes;
     bool bf16;
     float scale;
