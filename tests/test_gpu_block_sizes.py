@@ -128,3 +128,18 @@ def test_backward_block32_is_unsupported():
     with pytest.raises(tsa.TsaError) as e:
         tsa.tsa_scheduled_attention_backward(x, x, x, x, x, lse, rp, ci, 0.125, block=32)
     assert e.value.status == 2
+
+
+def test_autograd_block128_equals_explicit_calls():
+    from topology_scheduled_gb300.autograd import scheduled_attention
+    g = torch.Generator().manual_seed(9)
+    L, S, D = 2, 640, 64
+    q, k, v, dO = (torch.randn((L, S, D), generator=g).to(torch.bfloat16).to(DEV) for _ in range(4))
+    rp, ci = tsa.tsa_dense_causal_csr(S, 128)
+    qa, ka, va = (x.clone().requires_grad_(True) for x in (q, k, v))
+    out = scheduled_attention(qa, ka, va, rp, ci, 0.125, block=128)
+    out.backward(dO)
+    O, lse = tsa.tsa_scheduled_attention_fwd(q, k, v, rp, ci, 0.125, block=128)
+    dq, dk, dv = tsa.tsa_scheduled_attention_backward(q, k, v, O, dO, lse, rp, ci, 0.125, block=128)
+    assert torch.equal(out, O)
+    assert torch.equal(qa.grad, dq) and torch.equal(ka.grad, dk) and torch.equal(va.grad, dv)
