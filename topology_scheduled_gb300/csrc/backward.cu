@@ -391,20 +391,21 @@ __device__ __forceinline__ void copy_staged_row(const uint8_t *tile, int row, ui
 }
 
 // Meta area (byte offsets from the meta base), common to both kernels.
-constexpr int kBarTile = 0;        // resident tile(s) loaded
-constexpr int kBarFull = 8;        // kStream x 8: streamed block landed
-constexpr int kBarEmpty = 32;      // kStream x 8: streamed block released
-constexpr int kBarSFull = 56;      // 2 x 8: products of a step in TMEM
-constexpr int kBarPFull = 72;      // 2 x 8: elementwise results of a step in TMEM
-constexpr int kBarDone = 88;       // accumulation MMA of a step completed
-constexpr int kBarFin = 96;
-constexpr int kBarVFull = 104;     // dQ kernel: kStream x 8, V of a step landed
-constexpr int kBarVEmpty = 128;    // dQ kernel: kStream x 8
-constexpr int kTmemSlot = 152;
-constexpr int kAbortFlag = 156;
-constexpr int kMetaJ = 160;        // kMetaRing x 4
-constexpr int kMetaF = 176;        // kMetaRing x 4
+constexpr int kBarTile = 0;                           // resident tile(s) loaded
+constexpr int kBarFull = 8;                           // kStream x 8: streamed block landed
+constexpr int kBarEmpty = kBarFull + 8 * kStream;     // kStream x 8: streamed block released
+constexpr int kBarSFull = kBarEmpty + 8 * kStream;    // 2 x 8: products of a step in TMEM
+constexpr int kBarPFull = kBarSFull + 16;             // 2 x 8: elementwise results of a step in TMEM
+constexpr int kBarDone = kBarPFull + 16;              // accumulation MMA of a step completed
+constexpr int kBarFin = kBarDone + 8;
+constexpr int kBarVFull = kBarFin + 8;                // dQ kernel: kStream x 8, V of a step landed
+constexpr int kBarVEmpty = kBarVFull + 8 * kStream;   // dQ kernel: kStream x 8
+constexpr int kTmemSlot = kBarVEmpty + 8 * kStream;
+constexpr int kAbortFlag = kTmemSlot + 4;
+constexpr int kMetaJ = kAbortFlag + 4;                // kMetaRing x 4
+constexpr int kMetaF = kMetaJ + 4 * kMetaRing;        // kMetaRing x 4
 constexpr int kMetaBytes = 256;
+static_assert(kMetaF + 4 * kMetaRing <= kMetaBytes, "meta area");
 
 constexpr uint32_t kTmemCols = 512;  // S0 | S1 | dP0 | dP1 | accumulator(s)
 
@@ -651,8 +652,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t sr[32], pr[32];
-                    tmem_ld32(tmem + t_lane + s_col(u & 1) + h * 32, sr);
-                    tmem_ld32(tmem + t_lane + dp_col(u & 1) + h * 32, pr);
+                    tmem_ld32_pair(tmem + t_lane + s_col(u & 1) + h * 32, sr,
+                                   tmem + t_lane + dp_col(u & 1) + h * 32, pr);
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         float ds[2];
@@ -966,8 +967,8 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t sr[32], pr[32];
-                    tmem_ld32(tmem + t_lane + s_col(u & 1) + h * 32, sr);
-                    tmem_ld32(tmem + t_lane + dp_col(u & 1) + h * 32, pr);
+                    tmem_ld32_pair(tmem + t_lane + s_col(u & 1) + h * 32, sr,
+                                   tmem + t_lane + dp_col(u & 1) + h * 32, pr);
 #pragma unroll
                     for (int t = 0; t < 16; ++t) {
                         float p[2], ds[2];

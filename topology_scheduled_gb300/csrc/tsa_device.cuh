@@ -261,7 +261,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // Two TMEM loads of this warp's 32 lanes x 32 columns (columns taddr.. and taddr+32..) with a
 // single wait, so the two round trips overlap.
+// Two 32-column loads from unrelated TMEM addresses under one wait.
+__device__ __forceinline__ void tmem_ld32_pair(uint32_t taddr_r, uint32_t (&r)[32], uint32_t taddr_q,
+                                               uint32_t (&q)[32]);
+
 __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, uint32_t (&r)[32], uint32_t (&q)[32]) {
+    tmem_ld32_pair(taddr, r, taddr + 32, q);
+}
+
+__device__ __forceinline__ void tmem_ld32_pair(uint32_t taddr_r, uint32_t (&r)[32], uint32_t taddr_q,
+                                               uint32_t (&q)[32]) {
 #define TSA_LD32(dst, addr)                                                                            \
     asm volatile(                                                                                      \
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "                                                      \
@@ -282,8 +291,8 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t taddr, uint32_t (&r)[32], u
         "+r"(dst[19]), "+r"(dst[20]), "+r"(dst[21]), "+r"(dst[22]), "+r"(dst[23]), "+r"(dst[24]),      \
         "+r"(dst[25]), "+r"(dst[26]), "+r"(dst[27]), "+r"(dst[28]), "+r"(dst[29]), "+r"(dst[30]),      \
         "+r"(dst[31])
-    TSA_LD32(r, taddr);
-    TSA_LD32(q, taddr + 32);
+    TSA_LD32(r, taddr_r);
+    TSA_LD32(q, taddr_q);
     // the wait names both destinations so that no use or copy of them moves above it
     asm volatile("tcgen05.wait::ld.sync.aligned;" : TSA_HOLD32(r), TSA_HOLD32(q) : : "memory");
 #undef TSA_LD32
