@@ -526,21 +526,34 @@ def cpu_baseline_backward(args, w, q, k, v, dO, row_ptr, col_idx, nnz):
 
 
 def run_e2e(args, w, tsa, q, k, v, out, build, row_ptr, col_idx, topo, flops, stream, world):
-    """Same step through the public API from pinned host buffers, copies inside the timing."""
+    """Same step through the public API from pinned host buffers, copies inside the timing.
+    Topology schedules go through tsa_topology_attention_host (the C-ABI call that takes host
+    buffers and overlaps its copies with the build and the attention); the others copy with
+    torch around the device-resident calls."""
     steps = max(1, min(args.steps, 5))
     hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
     ho = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     hnnz = torch.empty(1, dtype=torch.int32, pin_memory=True)
+    host_call = args.schedule in ("topology", "topology-content")
+    if host_call:
+        ws = torch.empty(tsa.tsa_build_schedule_workspace_bytes(w.lanes, w.S, w.D, w.block),
+                         dtype=torch.uint8, device=q.device)
+        tie = "content" if args.schedule == "topology-content" else "index"
 
-    def step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        if topo:
-            build(row_ptr, col_idx)
-        tsa.tsa_scheduled_attention(q, k, v, row_ptr, col_idx, w.scale, out=out)
-        ho.copy_(out, non_blocking=True)
-        hnnz.copy_(row_ptr[-1:], non_blocking=True)
+        def step():
+            tsa.tsa_topology_attention_host(hq, hk, hv, w.block, w.sink, w.local_radius, w.topk, w.scale,
+                                            tie_break=tie, out=ho, device_buffers=(q, k, v, out),
+                                            row_ptr=row_ptr, col_idx=col_idx, workspace=ws)
+    else:
+        def step():
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+            if topo:
+                build(row_ptr, col_idx)
+            tsa.tsa_scheduled_attention(q, k, v, row_ptr, col_idx, w.scale, out=out)
+            ho.copy_(out, non_blocking=True)
+            hnnz.copy_(row_ptr[-1:], non_blocking=True)
 
     step()
     torch.cuda.synchronize()
@@ -552,10 +565,11 @@ def run_e2e(args, w, tsa, q, k, v, out, build, row_ptr, col_idx, topo, flops, st
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
     h2d = 3 * q.numel() * q.element_size()
-    d2h = out.numel() * out.element_size() + 4
+    d2h = out.numel() * out.element_size() + (0 if host_call else 4)
     return {"value": round(flops * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms, 3), "steps": steps,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "call": "tsa_topology_attention_host" if host_call else "torch copies + device calls"}
 
 
 def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo):

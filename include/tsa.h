@@ -334,6 +334,40 @@ tsa_status tsa_build_schedule_noalloc(const void *K, tsa_dtype dtype, int64_t la
                                       tsa_stream_t stream);
 
 /*
+ * One forward step of the path from HOST memory: the topology schedule built from K, the
+ * scheduled attention over it, and O back in host memory -- the calls above, with the
+ * host<->device copies overlapped with the work.  Lanes go in chunks of `lane_chunk` (0: an
+ * eighth of the lanes): the K chunks are copied first and each one's block sums run as soon
+ * as it lands, then the schedule; the Q and V chunks follow, each chunk's attention starts
+ * when its Q and V have landed, and its O is copied back on a third stream while the next
+ * chunk runs.  The copies use two streams of the library's own, created and released inside
+ * the call; the work runs on `stream`, and `stream` continues only after every copy has been
+ * made (the call is asynchronous like the others: synchronize `stream` before reading hO).
+ *
+ *   hQ, hK, hV   in, [B*H, S, D] of `dtype` in host memory (page-locked for the copies to run
+ *                asynchronously and overlap; pageable memory works, slower)
+ *   hO           out, host memory of the same shape
+ *   dQ, dK, dV, dO   device buffers of the same size, 16-byte aligned, not overlapping: the
+ *                device copies of the inputs and the device output (left valid after the call)
+ *   row_ptr, col_idx, col_cap, workspace, workspace_bytes, block, sink, local_radius, topk,
+ *                tie_break: as tsa_build_schedule_ex (workspace >=
+ *                tsa_build_schedule_workspace_bytes(B*H, S, D, block)); the schedule stays in
+ *                row_ptr / col_idx
+ *   scale        as tsa_scheduled_attention
+ *
+ * Limits: those of tsa_build_schedule_ex and tsa_scheduled_attention; at most 4096 chunks.
+ * Errors: INVALID_ARGUMENT (also for a device or managed pointer given as host memory),
+ * UNSUPPORTED, CAPACITY, NOT_DEVICE_POINTER, DEVICE_MISMATCH, CUDA.
+ */
+tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const void *hV, void *hO,
+                                       tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
+                                       int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
+                                       tsa_tie_break tie_break, float scale, void *dQ, void *dK, void *dV,
+                                       void *dO, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                                       void *workspace, size_t workspace_bytes, int64_t lane_chunk,
+                                       tsa_stream_t stream);
+
+/*
  * Synchronizes `stream`, then returns and clears the device status word of the current
  * device: TSA_OK, or the first of TIMEOUT, BAD_SCHEDULE, CAPACITY-on-device (reported as
  * TSA_ERR_DEVICE) raised by any call since the last read.  TSA_ERR_CUDA if the

@@ -21,7 +21,7 @@ def _declared():
 def test_every_declared_symbol_is_exported_and_bound():
     L = tsa.lib()
     names = _declared()
-    assert len(names) == 17
+    assert len(names) == 18
     for n in names:
         assert hasattr(L, n), n
         assert n in SIGNATURES, n
@@ -98,3 +98,30 @@ def test_fixed_segment_nnz_closed_form():
     assert tsa.tsa_fixed_segment_nnz(4096, 64, 1) == 64
     assert tsa.tsa_fixed_segment_nnz(4000, 64, 512) == -1
     assert tsa.tsa_fixed_segment_nnz(4096, 64, 0) == -1
+
+
+def test_host_step_argument_errors_need_no_gpu():
+    """tsa_topology_attention_host rejects bad arguments before touching the device."""
+    L = tsa.lib()
+    f = 4096  # any non-null, 256-byte aligned address: never dereferenced on these paths
+    m = 1 << 20  # distinct device buffers (128 KB each here), so that they do not overlap
+    args = [f, f, f, f, 1, 1, 1, 1024, 64, 64, 1, 1, 2, 0, 0.125, f, f + m, f + 2 * m, f + 3 * m, f, f, 1000, f,
+            1 << 30, 0, None]
+    a = list(args); a[0] = None
+    assert L.tsa_topology_attention_host(*a) == 1          # null host pointer
+    a = list(args); a[4] = 7
+    assert L.tsa_topology_attention_host(*a) == 1          # unknown dtype
+    a = list(args); a[13] = 9
+    assert L.tsa_topology_attention_host(*a) == 1          # unknown tie rule
+    a = list(args); a[9] = 16
+    assert L.tsa_topology_attention_host(*a) == 2          # block 16
+    a = list(args); a[8] = 96
+    assert L.tsa_topology_attention_host(*a) == 2          # head dim 96
+    a = list(args); a[24] = -1
+    assert L.tsa_topology_attention_host(*a) == 1          # negative lane chunk
+    a = list(args); a[16] = f + 8
+    assert L.tsa_topology_attention_host(*a) == 1          # misaligned device buffer
+    a = list(args); a[17] = f + (64 << 10)  # inside dQ
+    assert L.tsa_topology_attention_host(*a) == 1          # overlapping device buffers
+    a = list(args); a[21] = 5
+    assert L.tsa_topology_attention_host(*a) == 5          # CSR capacity below the bound (70)

@@ -58,6 +58,9 @@ SIGNATURES = {
     "tsa_scheduled_attention_backward": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P,
                                                         ctypes.c_int, _I64, _I64, _I64, _I64, _I64,
                                                         ctypes.c_float, _P, _SZ, _P]),
+    "tsa_topology_attention_host": (ctypes.c_int, [_P, _P, _P, _P, ctypes.c_int, _I64, _I64, _I64, _I64,
+                                                   _I64, _I64, _I64, _I64, ctypes.c_int, ctypes.c_float,
+                                                   _P, _P, _P, _P, _P, _P, _I64, _P, _SZ, _I64, _P]),
 }
 
 
@@ -359,3 +362,54 @@ def tsa_scheduled_attention_backward(Q, K, V, O, dO, lse, row_ptr, col_idx, scal
 def tsa_last_device_status(stream=None) -> int:
     """Synchronizes the stream; returns and clears the device status word (0 = TSA_OK)."""
     return int(lib().tsa_last_device_status(_stream(stream)))
+
+
+def tsa_topology_attention_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, block: int = 64,
+                                sink: int = 1, local_radius: int = 1, topk: int = 2, scale: float | None = None,
+                                *, tie_break: str = "index", out: torch.Tensor | None = None,
+                                device_buffers=None, row_ptr: torch.Tensor | None = None,
+                                col_idx: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                                lane_chunk: int = 0, device=None, stream=None):
+    """One forward step from host tensors ([S, D], [L, S, D] or [B, H, S, D]; page-locked for
+    the copies to overlap): the topology CSR from K and the scheduled attention, O returned in
+    host memory (``out``, page-locked if not given).  ``device_buffers`` = (dQ, dK, dV, dO) on
+    the device; allocated when not given.  Returns (out, row_ptr, col_idx); the call is
+    asynchronous on ``stream`` like the others."""
+    for name, t in (("hQ", hQ), ("hK", hK), ("hV", hV)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if not (hQ.shape == hK.shape == hV.shape and hQ.dtype == hK.dtype == hV.dtype):
+        raise ValueError("hQ, hK, hV must share shape and dtype")
+    if tie_break not in TIE_RULES:
+        raise ValueError(f"tie_break must be one of {sorted(TIE_RULES)}")
+    B, H, S, D = _lanes_S_D(hQ)
+    lanes = B * H
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    L = lib()
+    nb = -(-S // block) if block > 0 else 0
+    cap = int(L.tsa_schedule_max_nnz(S, block, sink, local_radius, topk))
+    if cap < 0:
+        raise TsaError(1, "tsa_schedule_max_nnz")
+    ws_bytes = int(L.tsa_build_schedule_workspace_bytes(lanes, S, D, block))
+    if ws_bytes == 0:
+        raise TsaError(2, "tsa_build_schedule_workspace_bytes")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if row_ptr is None:
+        row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+    if col_idx is None:
+        col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    if device_buffers is None:
+        device_buffers = tuple(torch.empty(hQ.shape, dtype=hQ.dtype, device=dev) for _ in range(4))
+    if out is None:
+        out = torch.empty(hQ.shape, dtype=hQ.dtype, pin_memory=True)
+    dq, dk, dv, do = device_buffers
+    _check(L.tsa_topology_attention_host(hQ.data_ptr(), hK.data_ptr(), hV.data_ptr(), out.data_ptr(),
+                                         _dtype_code(hQ), B, H, S, D, block, sink, local_radius, topk,
+                                         TIE_RULES[tie_break], float(scale), dq.data_ptr(), dk.data_ptr(),
+                                         dv.data_ptr(), do.data_ptr(), row_ptr.data_ptr(), col_idx.data_ptr(),
+                                         col_idx.numel(), workspace.data_ptr(), workspace.numel(), int(lane_chunk),
+                                         _stream(stream)), "tsa_topology_attention_host")
+    return out, row_ptr, col_idx

@@ -4,6 +4,7 @@
 #include <climits>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "tsa_internal.h"
 
@@ -121,6 +122,11 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
 }
+
+tsa_status launch_attention_checked(const void *Q, const void *K, const void *V, const int32_t *row_ptr,
+                                    const int32_t *col_idx, void *O, float *lse, bool bf16, int64_t lanes,
+                                    int64_t S, int64_t D, int64_t block, float scale, cudaStream_t stream,
+                                    int dev);
 
 int64_t max_nnz_bound(int64_t nb, int64_t sink, int64_t r, int64_t topk) {
     // sum_{i < nb} min(i + 1, per), per = sink + r + 1 + topk (saturating at nb)
@@ -395,7 +401,19 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
                           static_cast<const void *>(col_idx)})
         TSA_TRY(check_device_ptr(p, dev));
     if (lse) TSA_TRY(check_device_ptr(lse, dev));
-    const bool bf16 = dtype == TSA_BF16;
+    return launch_attention_checked(Q, K, V, row_ptr, col_idx, O, lse, dtype == TSA_BF16, lanes, S, D, block,
+                                    scale, reinterpret_cast<cudaStream_t>(stream), dev);
+}
+
+}  // extern "C"
+
+namespace tsa {
+namespace {
+// The attention launch once the arguments have been checked.
+tsa_status launch_attention_checked(const void *Q, const void *K, const void *V, const int32_t *row_ptr,
+                                    const int32_t *col_idx, void *O, float *lse, bool bf16, int64_t lanes,
+                                    int64_t S, int64_t D, int64_t block, float scale, cudaStream_t stream,
+                                    int dev) {
     const uint64_t rows = (uint64_t)(lanes * S);
     CUtensorMap tmQ, tmK, tmV, tmO;
     if (!encode_2d(&tmQ, Q, bf16, rows, (uint64_t)D, 128) || !encode_2d(&tmK, K, bf16, rows, (uint64_t)D, 64) ||
@@ -417,10 +435,14 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
     a.lanes = (int)lanes;
     a.bf16 = bf16;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
-    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    a.stream = stream;
     TSA_TRY(device_flags(dev, &a.flags));
     return launch_scheduled_attention(a);
 }
+}  // namespace
+}  // namespace tsa
+
+extern "C" {
 
 size_t tsa_attention_backward_workspace_bytes(int64_t lanes, int64_t S, int64_t block, int64_t nnz_cap) {
     if (lanes <= 0 || S <= 0 || (block != 64 && block != 128) || nnz_cap < 1) return 0;
@@ -546,6 +568,156 @@ tsa_status tsa_last_device_status(tsa_stream_t stream) {
     if (bits & kDevBadSchedule) return TSA_ERR_BAD_SCHEDULE;
     if (bits) return TSA_ERR_DEVICE;
     return TSA_OK;
+}
+
+
+// One forward step from host memory, copies overlapped with the work (see include/tsa.h).
+tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const void *hV, void *hO,
+                                       tsa_dtype dtype, int64_t B, int64_t H, int64_t S, int64_t D,
+                                       int64_t block, int64_t sink, int64_t local_radius, int64_t topk,
+                                       tsa_tie_break tie_break, float scale, void *dQ, void *dK, void *dV,
+                                       void *dO, int32_t *row_ptr, int32_t *col_idx, int64_t col_cap,
+                                       void *workspace, size_t workspace_bytes, int64_t lane_chunk,
+                                       tsa_stream_t stream) {
+    if (!hQ || !hK || !hV || !hO || !dQ || !dK || !dV || !dO || !row_ptr || !col_idx || !workspace)
+        return TSA_ERR_INVALID_ARGUMENT;
+    if (dtype != TSA_F16 && dtype != TSA_BF16) return TSA_ERR_INVALID_ARGUMENT;
+    if (tie_break != TSA_TIE_INDEX && tie_break != TSA_TIE_CONTENT) return TSA_ERR_INVALID_ARGUMENT;
+    if (B <= 0 || H <= 0 || S <= 0 || D <= 0 || block <= 0 || lane_chunk < 0) return TSA_ERR_INVALID_ARGUMENT;
+    if (sink < 0 || local_radius < 0 || topk < 0 || !std::isfinite(scale)) return TSA_ERR_INVALID_ARGUMENT;
+    if ((block != 32 && block != 64 && block != 128) || (D != 64 && D != 128)) return TSA_ERR_UNSUPPORTED;
+    if (B > 65535 || H > 65535 || B * H > 65535) return TSA_ERR_UNSUPPORTED;
+    const int64_t lanes = B * H;
+    if (lanes * S >= (int64_t)INT_MAX) return TSA_ERR_UNSUPPORTED;
+    const int64_t nb = (S + block - 1) / block;
+    if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
+    void *dev_bufs[] = {dQ, dK, dV, dO};
+    for (void *p : dev_bufs)
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return TSA_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return TSA_ERR_INVALID_ARGUMENT;
+    const size_t bytes = (size_t)(lanes * S * D) * 2;
+    for (int x = 0; x < 4; ++x)
+        for (int y = x + 1; y < 4; ++y)
+            if (overlaps(dev_bufs[x], bytes, dev_bufs[y], bytes)) return TSA_ERR_INVALID_ARGUMENT;
+    if (col_cap < max_nnz_bound(nb, sink, local_radius, topk)) return TSA_ERR_CAPACITY;
+    const ScheduleWorkspace ws = schedule_workspace_layout(lanes, nb, D);
+    if (workspace_bytes < ws.total) return TSA_ERR_CAPACITY;
+    int dev;
+    TSA_TRY(current_device(&dev));
+    for (void *p : dev_bufs) TSA_TRY(check_device_ptr(p, dev));
+    for (const void *p : {static_cast<const void *>(row_ptr), static_cast<const void *>(col_idx),
+                          static_cast<const void *>(workspace)})
+        TSA_TRY(check_device_ptr(p, dev));
+    // the host side must be host memory (pinned for the copies to overlap; pageable works too)
+    for (const void *p : {hQ, hK, hV, static_cast<const void *>(hO)}) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+            cudaGetLastError();
+            return TSA_ERR_INVALID_ARGUMENT;
+        }
+        if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return TSA_ERR_INVALID_ARGUMENT;
+    }
+    const bool bf16 = dtype == TSA_BF16;
+    const int64_t lc = lane_chunk > 0 ? (lane_chunk < lanes ? lane_chunk : lanes) : (lanes + 7) / 8;
+    const int64_t nchunks = (lanes + lc - 1) / lc;
+    if (nchunks > 4096) return TSA_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    DeviceFlags flags;
+    TSA_TRY(device_flags(dev, &flags));
+
+    // Two copy streams beside the caller's: host-to-device (K first, then Q and V) and
+    // device-to-host (O).  The work itself runs on the caller's stream.  Streams and events are
+    // released right after enqueueing; CUDA keeps them until their work has completed.
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    std::vector<cudaEvent_t> ev;
+    auto cleanup = [&]() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+        if (s_in) cudaStreamDestroy(s_in);
+        if (s_out) cudaStreamDestroy(s_out);
+    };
+    auto event = [&](cudaEvent_t *e) {
+        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+        ev.push_back(*e);
+        return true;
+    };
+    const size_t lane_bytes = (size_t)(S * D) * 2;
+    auto chunk = [&](const void *base, int64_t c) {
+        return static_cast<const uint8_t *>(base) + (size_t)(c * lc) * lane_bytes;
+    };
+    auto chunk_lanes = [&](int64_t c) { return (c + 1) * lc <= lanes ? lc : lanes - c * lc; };
+    bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess;
+    cudaEvent_t e_start = nullptr, e_end = nullptr;
+    ok = ok && event(&e_start) && event(&e_end) && cudaEventRecord(e_start, st) == cudaSuccess &&
+         cudaStreamWaitEvent(s_in, e_start, 0) == cudaSuccess && cudaStreamWaitEvent(s_out, e_start, 0) == cudaSuccess;
+    std::vector<cudaEvent_t> e_k(nchunks), e_qv(nchunks), e_o(nchunks);
+    for (int64_t c = 0; ok && c < nchunks; ++c) {
+        const size_t n = (size_t)chunk_lanes(c) * lane_bytes;
+        ok = event(&e_k[c]) &&
+             cudaMemcpyAsync((void *)chunk(dK, c), chunk(hK, c), n, cudaMemcpyHostToDevice, s_in) == cudaSuccess &&
+             cudaEventRecord(e_k[c], s_in) == cudaSuccess;
+    }
+    for (int64_t c = 0; ok && c < nchunks; ++c) {
+        const size_t n = (size_t)chunk_lanes(c) * lane_bytes;
+        ok = event(&e_qv[c]) &&
+             cudaMemcpyAsync((void *)chunk(dQ, c), chunk(hQ, c), n, cudaMemcpyHostToDevice, s_in) == cudaSuccess &&
+             cudaMemcpyAsync((void *)chunk(dV, c), chunk(hV, c), n, cudaMemcpyHostToDevice, s_in) == cudaSuccess &&
+             cudaEventRecord(e_qv[c], s_in) == cudaSuccess;
+    }
+    // the schedule: per-lane block sums as each K chunk lands, then the lane mean and the graph
+    ScheduleLaunch a{};
+    a.K = static_cast<const uint16_t *>(dK);
+    a.bf16 = bf16;
+    a.lanes = lanes;
+    a.S = S;
+    a.D = D;
+    a.block = block;
+    a.nb = nb;
+    a.sink = sink < nb ? sink : nb;
+    a.local_radius = local_radius < nb ? local_radius : nb;
+    a.topk = topk < nb ? topk : nb;
+    a.content_ties = tie_break == TSA_TIE_CONTENT;
+    a.row_ptr = row_ptr;
+    a.col_idx = col_idx;
+    a.col_cap = col_cap;
+    a.salience_sq = nullptr;
+    a.workspace = static_cast<uint8_t *>(workspace);
+    a.stream = st;
+    a.flags = flags;
+    double *part = reinterpret_cast<double *>(a.workspace + ws.part);
+    tsa_status status = ok ? TSA_OK : TSA_ERR_CUDA;
+    for (int64_t c = 0; status == TSA_OK && c < nchunks; ++c) {
+        if (cudaStreamWaitEvent(st, e_k[c], 0) != cudaSuccess) { status = TSA_ERR_CUDA; break; }
+        ScheduleLaunch ac = a;
+        ac.K = reinterpret_cast<const uint16_t *>(chunk(dK, c));
+        ac.lanes = chunk_lanes(c);
+        status = launch_block_sums(ac, part + (size_t)(c * lc) * (size_t)(nb * D));
+    }
+    if (status == TSA_OK) status = launch_schedule_from_sums(a, part);
+    // attention per lane chunk as its Q and V land; its O goes back while the next one runs
+    for (int64_t c = 0; status == TSA_OK && c < nchunks; ++c) {
+        if (cudaStreamWaitEvent(st, e_qv[c], 0) != cudaSuccess) { status = TSA_ERR_CUDA; break; }
+        status = launch_attention_checked(chunk(dQ, c), chunk(dK, c), chunk(dV, c), row_ptr, col_idx,
+                                          (void *)chunk(dO, c), nullptr, bf16, chunk_lanes(c), S, D, block,
+                                          scale, st, dev);
+        if (status != TSA_OK) break;
+        const size_t n = (size_t)chunk_lanes(c) * lane_bytes;
+        if (!event(&e_o[c]) || cudaEventRecord(e_o[c], st) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, e_o[c], 0) != cudaSuccess ||
+            cudaMemcpyAsync((void *)chunk(hO, c), chunk(dO, c), n, cudaMemcpyDeviceToHost, s_out) != cudaSuccess)
+            status = TSA_ERR_CUDA;
+    }
+    // the caller's stream continues once every copy has been made
+    if (s_in && s_out && e_end) {
+        cudaEvent_t e_in = nullptr;
+        if (!event(&e_in) || cudaEventRecord(e_in, s_in) != cudaSuccess ||
+            cudaStreamWaitEvent(s_out, e_in, 0) != cudaSuccess || cudaEventRecord(e_end, s_out) != cudaSuccess ||
+            cudaStreamWaitEvent(st, e_end, 0) != cudaSuccess)
+            status = TSA_ERR_CUDA;
+    }
+    cleanup();
+    if (status != TSA_OK) cudaGetLastError();
+    return status;
 }
 
 }  // extern "C"
