@@ -336,8 +336,8 @@ tsa_status tsa_build_schedule_noalloc(const void *K, tsa_dtype dtype, int64_t la
 /*
  * One forward step of the path from HOST memory: the topology schedule built from K, the
  * scheduled attention over it, and O back in host memory -- the calls above, with the
- * host<->device copies overlapped with the work.  Lanes go in chunks of `lane_chunk` (0: an
- * eighth of the lanes): the K chunks are copied first and each one's block sums run as soon
+ * host<->device copies overlapped with the work.  Lanes go in chunks of `lane_chunk` (0: a
+ * sixteenth of the lanes): the K chunks are copied first and each one's block sums run as soon
  * as it lands, then the schedule; the Q and V chunks follow, each chunk's attention starts
  * when its Q and V have landed, and its O is copied back on a third stream while the next
  * chunk runs.  The copies use two streams of the library's own, created and released inside

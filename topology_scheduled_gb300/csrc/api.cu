@@ -618,7 +618,7 @@ tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const voi
         if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return TSA_ERR_INVALID_ARGUMENT;
     }
     const bool bf16 = dtype == TSA_BF16;
-    const int64_t lc = lane_chunk > 0 ? (lane_chunk < lanes ? lane_chunk : lanes) : (lanes + 7) / 8;
+    const int64_t lc = lane_chunk > 0 ? (lane_chunk < lanes ? lane_chunk : lanes) : (lanes + 15) / 16;
     const int64_t nchunks = (lanes + lc - 1) / lc;
     if (nchunks > 4096) return TSA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
