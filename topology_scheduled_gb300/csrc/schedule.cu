@@ -114,26 +114,14 @@ __device__ double column_sum_exact_slow(const uint16_t *src, int64_t D, int64_t 
     return acc;
 }
 
-// One thread per (lane, block, 8 consecutive d); 16-byte loads.
-//
-// bf16 fast path: the column is summed as an unevaluated pair hi + lo of fp32 values (packed
-// two columns at a time).  Each step is Knuth's TwoSum, which splits hi + x exactly into the
-// rounded sum and its error; the errors collect in lo.  Every element and every error is an
-// integer multiple of 2^(e_min - 134), each error is below 2^(e_max - 143) in magnitude, so
-// lo's partial sums (64 of them) need at most e_max - e_min - 4 significant bits: with
-// e_max - e_min <= 28 (biased exponents of the non-zero elements, from the packed 16-bit
-// max/min of |bits|; subnormals count as exponent 1; no inf/nan) lo is exact, hence
-// hi + lo is the exact column sum.  That sum has at most e_max - e_min + 14 <= 42 significant
-// bits, so the sequential binary64 sum is exact too and both equal (double)hi + (double)lo.
-// Other columns (and f16, and blocks longer than 64) take the int64 path above.
-// Two CTAs of 256 threads per SM (at most 128 registers): this pass is bound by the HBM
-// read of K, and occupancy is what keeps enough loads in flight.
+// One thread per (lane, block, 8 consecutive d); 16-byte loads; the int64 path above.  Used
+// for bf16 keys in blocks longer than 64 tokens (the TwoSum bound below covers 64 terms); the
+// streamed kernel further down takes every other 16-byte-aligned case.
 __global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
                                       int64_t S, int64_t D, int64_t block, int64_t nb,
                                       int spread_limit, double *__restrict__ part) {
     const int64_t groups = D / 8;
     const int64_t total = lanes * nb * groups;
-    const bool fp32_path = bf16 && block <= 64;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < total;
          w += (int64_t)gridDim.x * blockDim.x) {
         const int64_t g = w % groups;
@@ -142,67 +130,6 @@ __global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *
         const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
         const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
         double *dst = part + lb * D + g * 8;
-        if (fp32_path) {
-            uint64_t hi[4], lo[4];
-            uint32_t mx[4], mn[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                hi[i] = f2_pack(0.f, 0.f);
-                lo[i] = hi[i];
-                mx[i] = 0u;
-                mn[i] = 0xFFFFFFFFu;
-            }
-            // hi + lo += x exactly (TwoSum), two columns per packed operation
-            auto two_sum = [&](int i, uint32_t x) {
-                const uint64_t v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
-                const uint64_t s = f2_add(hi[i], v);
-                const uint64_t bv = f2_sub(s, hi[i]);
-                const uint64_t err = f2_add(f2_sub(hi[i], f2_sub(s, bv)), f2_sub(v, bv));
-                lo[i] = f2_add(lo[i], err);
-                hi[i] = s;
-                const uint32_t a = x & 0x7FFF7FFFu;
-                mx[i] = __vmaxu2(mx[i], a);
-                mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
-            };
-            int64_t t = 0;
-            for (; t + 8 <= n; t += 8) {
-                uint4 v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) v[u] = __ldg(reinterpret_cast<const uint4 *>(src + (t + u) * D));
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    two_sum(0, v[u].x);
-                    two_sum(1, v[u].y);
-                    two_sum(2, v[u].z);
-                    two_sum(3, v[u].w);
-                }
-            }
-            for (; t < n; ++t) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
-                two_sum(0, v.x);
-                two_sum(1, v.y);
-                two_sum(2, v.z);
-                two_sum(3, v.w);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float h0, h1, l0, l1;
-                f2_unpack(hi[i], h0, h1);
-                f2_unpack(lo[i], l0, l1);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
-                    const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
-                    const int emax = (int)(amax >> 7);
-                    const int emin = max(1, (int)(amin >> 7));
-                    const bool all_zero = amin == 0xFFFFu;
-                    const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
-                    dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
-                                           : column_sum_exact_slow(src + 2 * i + h, D, n, bf16, spread_limit);
-                }
-            }
-            continue;
-        }
         ColumnSum c[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) col_init(c[i]);
@@ -243,12 +170,23 @@ __global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *
     }
 }
 
-// centroid_partial_vec8's arithmetic (same items, same per-column arithmetic in the same token
-// order, so the same bits), streamed: each thread copies its next rows of 16 bytes into shared
-// memory with cp.async while it sums earlier ones, so a thread always has loads in flight
-// instead of alternating between loading and summing.  The staging area is
-// [stage][row][thread] (16-byte words), so the 32 lanes of a warp touch consecutive words.
-// bf16 keys sum by TwoSum (blocks of at most 64 tokens), f16 keys by the int64 path.
+// Block sums with 16-byte rows streamed: each thread copies its next rows into shared memory
+// with cp.async while it sums earlier ones, so a thread always has loads in flight instead of
+// alternating between loading and summing.  The staging area is [stage][row][thread]
+// (16-byte words), so the 32 lanes of a warp touch consecutive words.  One thread per (lane,
+// block, 8 consecutive d); tokens in ascending order.  f16 keys take the int64 path above.
+//
+// bf16 fast path: the column is summed as an unevaluated pair hi + lo of fp32 values (packed
+// two columns at a time).  Each step is Knuth's TwoSum, which splits hi + x exactly into the
+// rounded sum and its error; the errors collect in lo.  Every element and every error is an
+// integer multiple of 2^(e_min - 134), each error is below 2^(e_max - 143) in magnitude, so
+// lo's partial sums (64 of them) need at most e_max - e_min - 4 significant bits: with
+// e_max - e_min <= 28 (biased exponents of the non-zero elements, from the packed 16-bit
+// max/min of |bits|; subnormals count as exponent 1; no inf/nan) lo is exact, hence
+// hi + lo is the exact column sum.  That sum has at most e_max - e_min + 14 <= 42 significant
+// bits, so the sequential binary64 sum is exact too and both equal (double)hi + (double)lo.
+// Other columns take the sequential binary64 loop (column_sum_exact_slow).
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
