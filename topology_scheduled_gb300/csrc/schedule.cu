@@ -592,16 +592,20 @@ __device__ bool grid_sync(unsigned *gbar, const DeviceFlags &f) {
     return s_ok != 0;
 }
 
+// The strict edge order (d2, min(u,v), max(u,v)).  Squared distances are sums of squares from
+// +0, never negative zero or NaN (or the +inf sentinel), so their bit patterns order like their
+// values: the comparison runs on the integer pipe, not on this part's slow FP64 one.
 __device__ __forceinline__ bool key_less(double d1, int a1, int b1, double d2, int a2, int b2) {
-    if (d1 < d2) return true;
-    if (d1 > d2) return false;
+    const unsigned long long u1 = (unsigned long long)__double_as_longlong(d1);
+    const unsigned long long u2 = (unsigned long long)__double_as_longlong(d2);
+    if (u1 != u2) return u1 < u2;
     if (a1 != a2) return a1 < a2;
     return b1 < b2;
 }
 
 // Each vertex's lightest edge to another component; one warp per vertex, grid-wide.  Every
 // CTA keeps its own copy of the component labels in shared memory (`scomp`); each lane reads
-// its d2 entries in independent batches of 8.
+// its d2 entries in independent batches of 16 (one batch covers a 512-block row).
 __device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, double *vb_d, int *vb_u) {
     const int nb = a.nb;
     const int lane = threadIdx.x & 31;
@@ -612,15 +616,15 @@ __device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, double *v
         double bd = __longlong_as_double((long long)kInfBits);
         int ba = INT_MAX, bb = INT_MAX, bu = -1;
         const double *row = a.d2 + (int64_t)v * nb;
-        for (int u0 = lane; u0 < nb; u0 += 32 * 8) {
-            double d[8];
+        for (int u0 = lane; u0 < nb; u0 += 32 * 16) {
+            double d[16];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 const int u = u0 + 32 * k;
                 d[k] = u < nb ? __ldg(row + u) : 0.0;
             }
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 const int u = u0 + 32 * k;
                 if (u < nb && scomp[u] != cv) {
                     const int x = u < v ? u : v, y = u < v ? v : u;
