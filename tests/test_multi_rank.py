@@ -30,7 +30,7 @@ def _rank(rank, world, port, out):
 def test_two_ranks_take_max_time_and_sum_work():
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
@@ -76,7 +76,7 @@ def test_lane_sharded_block_sums_gather_in_lane_order(cuts):
     lane-mean centroid."""
     world = 2
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_shard_rank, args=(world, port, cuts, out), nprocs=world, join=True)
         res = dict(out)
