@@ -170,17 +170,27 @@ int oracle_centroids(const uint16_t *K, int dtype, int64_t L, int64_t S, int64_t
 
 /*
  * Reading: the distance is Euclidean; every comparison uses its square,
- *   d2(u,v) = sum_{d=0}^{D-1} (C[u][d] - C[v][d])^2
- * accumulated in ascending d with one fused multiply-add per term.
+ *   d2(u,v) = sum_{d=0}^{D-1} (C[u][d] - C[v][d])^2,
+ * in binary64 with one fixed order of summation (the pages fix none):
+ *   P_j = the terms d = j, j + 32, j + 64, ... (d < D) accumulated in ascending
+ *         d from +0 with one fused multiply-add each, for j = 0 .. 31;
+ *   then halving: P_j = P_j + P_{j+w} for j < w, w = 16, 8, 4, 2, 1; d2 = P_0.
+ * (An empty P_j is +0, and adding +0 changes no sum.)
  */
 static double pair_d2(const double *C, int64_t D, int64_t u, int64_t v)
 {
-    double acc = 0.0;
-    for (int64_t d = 0; d < D; ++d) {
-        double delta = C[u * D + d] - C[v * D + d];
-        acc = fma(delta, delta, acc);
+    double part[32];
+    for (int j = 0; j < 32; ++j) {
+        double acc = 0.0;
+        for (int64_t d = j; d < D; d += 32) {
+            double delta = C[u * D + d] - C[v * D + d];
+            acc = fma(delta, delta, acc);
+        }
+        part[j] = acc;
     }
-    return acc;
+    for (int w = 16; w >= 1; w /= 2)
+        for (int j = 0; j < w; ++j) part[j] = part[j] + part[j + w];
+    return part[0];
 }
 
 int oracle_pairwise_d2(const double *C, int64_t nb, int64_t D, double *D2)

@@ -89,6 +89,44 @@ def test_pairwise_d2_matches_scipy_and_is_symmetric():
     np.testing.assert_allclose(D2, cdist(C, C, "sqeuclidean"), rtol=1e-13, atol=1e-12)
 
 
+def test_pairwise_d2_summation_order():
+    """The stated binary64 order, written out with exact rationals (each fused multiply-add and
+    each addition rounded once): 32 strided partial sums, then halving.  Coordinates spread over
+    many binades so that a sequential sum rounds differently; D = 1, 31, 32, 33 and 100 cover
+    empty, single-term and uneven partial sums."""
+    from fractions import Fraction
+
+    def fma(a, b, c):
+        return float(Fraction(a) * Fraction(b) + Fraction(c))
+
+    def add(a, b):
+        return float(Fraction(a) + Fraction(b))
+
+    g = np.random.default_rng(17)
+    seq_differs = 0
+    for D in (1, 31, 32, 33, 100):
+        C = g.normal(size=(4, D)) * np.exp2(g.integers(-30, 30, size=(4, D)))
+        D2 = oracle.pairwise_d2(C)
+        for u, v in ((0, 1), (2, 3), (1, 3)):
+            delta = [float(C[u, d] - C[v, d]) for d in range(D)]
+            part = []
+            for j in range(32):
+                acc = 0.0
+                for d in range(j, D, 32):
+                    acc = fma(delta[d], delta[d], acc)
+                part.append(acc)
+            w = 16
+            while w >= 1:
+                part = [add(part[j], part[j + w]) for j in range(w)] + part[w:]
+                w //= 2
+            assert D2[u, v] == part[0] and D2[v, u] == part[0]
+            seq = 0.0
+            for d in range(D):
+                seq = fma(delta[d], delta[d], seq)
+            seq_differs += seq != part[0]
+    assert seq_differs > 0  # the inputs do tell the two orders apart
+
+
 # ---------------------------------------------------------------- salience
 def _golden_elder():
     cases, csr = [], None
