@@ -95,7 +95,7 @@ def aggregate_over_ranks(elapsed_ms: float, flops: float, device, world: int):
 
 def launches_per_step(schedule: str) -> int:
     """Kernels of this library per step: the attention kernel, plus the builder's kernels when
-    the schedule is built inside the step -- centroid_partial, centroid_final, pairwise_d2 and
+    the schedule is built inside the step -- centroid_partial, centroid_final, pairwise_bounds and
     the cooperative graph kernel for a topology schedule (content_rank and permute_rows in
     addition under content ties), segment_rows and segment_fill for fixed segments."""
     return 1 + {"topology": 4, "topology-content": 6}.get(

@@ -83,7 +83,7 @@ int64_t tsa_schedule_max_nnz(int64_t S, int64_t block, int64_t sink, int64_t loc
 
 /*
  * Bytes of device workspace tsa_build_schedule needs for `lanes` lanes of [S, D] keys
- * (per-lane block sums, centroids, the pairwise distance matrix and MST state).
+ * (per-lane block sums, centroids, the pairwise distance intervals and MST state).
  * Returns 0 for invalid arguments.
  */
 size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, int64_t block);
@@ -96,7 +96,9 @@ size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, i
  *   K            [lanes, S, D] keys (f16 or bf16 per dtype).
  *   centroids    C[b][d] = (sum_lanes (sum_{t in block b} K)) / (block * lanes), binary64,
  *                both sums sequential in ascending order.
- *   distance     d2(u,v) = sum_d (C[u][d] - C[v][d])^2, ascending d, fused multiply-add.
+ *   distance     d2(u,v) = sum_d (C[u][d] - C[v][d])^2 in binary64: 32 partial sums over
+ *                d = j mod 32 (ascending d, one fused multiply-add per term), then halving
+ *                (P_j += P_{j+w}, w = 16, 8, 4, 2, 1).
  *   salience     Kruskal order on edges (d2, min(u,v), max(u,v)); the smaller component is
  *                absorbed, on a size tie the one whose root has the larger index; the
  *                absorbed root gets the edge's d2 (squared merge distance); one block keeps 0.

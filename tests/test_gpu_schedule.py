@@ -108,6 +108,28 @@ def test_random_small_and_ragged(seed):
                  distinct=(seed % 3 != 0 and seed % 4 != 1 and D * block > 2))
 
 
+@pytest.mark.parametrize("nb,dtype,jmax", [(40, torch.float16, 4), (300, torch.float16, 1024),
+                                           (300, torch.bfloat16, 4)])
+def test_distances_below_binary32_resolution(nb, dtype, jmax):
+    """Blocks of two tokens, (2048, ...) and (j * 2^-14, ...): centroids 1024 + j * 2^-15, whose
+    last bits lie below the binary32 resolution at 1024 (2^-13).  With j < 4 the rows collapse
+    to a handful of binary32 values (and a few dozen binary64 ones, so exact ties abound); with
+    j < 1024 they stay apart but a binary32 difference can be off by half its size.  Either way the binary32
+    distance intervals cannot order the edges and the binary64 keys decide.  Every 7th block
+    sits at -2048, so that some edges are excluded by their bounds.  Covers the per-pair
+    interval kernel (nb < 256) and the tiled one."""
+    D, block = 3, 2
+    g = torch.Generator().manual_seed(nb + jmax)
+    x = torch.zeros((1, nb * block, D))
+    x[0, 0::2] = 2048.0
+    x[0, 0::14] = -2048.0
+    x[0, 1::2] = torch.randint(0, jmax, (nb, D), generator=g).float() * 2.0 ** -14
+    k = x.to(dtype)
+    assert torch.equal(k.float(), x)  # every key exact in the key format
+    kd = k.to(DEV)
+    _assert_same(_gpu_schedule(kd, block, 1, 2, 4), _oracle_schedule(kd, block, 1, 2, 4), distinct=False)
+
+
 def test_largest_block_count():
     nb = 4096
     gen = torch.Generator().manual_seed(7)

@@ -10,16 +10,22 @@
 //
 // The result is bit-identical to the CPU oracle because every floating-point step is fixed:
 //   C[b][d]  = (sum over lanes of (sum over the block's tokens, ascending)) / (block * lanes)
-//   d2(u,v)  = fma-accumulated sum of (C[u][d] - C[v][d])^2 over ascending d
+//   d2(u,v)  = sum of (C[u][d] - C[v][d])^2 in a fixed order: 32 partial sums over
+//              d = j mod 32 (ascending, fused multiply-add), then halving
 //   ordering = strict key (d2, min(u,v), max(u,v)), so the MST is unique and Boruvka here
 //              selects the same tree as Kruskal in the oracle.
 //
 // Kernels, in stream order:
 //   centroid_partial      per (lane, block, d): sum of the block's tokens   (HBM stream of K)
-//   centroid_final        per (block, d): sum over lanes, divide             (small)
-//   pairwise_d2           nb x nb squared distances over the upper triangle  (FP64 ALU)
-//   schedule_graph_kernel one cooperative launch: Boruvka MST, elder-rule salience, top-k
-//                         CSR (see the section comment below)
+//   centroid_final        per (block, d): sum over lanes, divide; also the binary32 copy
+//   pairwise_bounds       per pair: an interval [lo, hi] that provably holds the binary64
+//                         d2, from binary32 arithmetic                       (FP32 ALU)
+//   schedule_graph_kernel one cooperative launch: Boruvka MST (exact binary64 d2 only for
+//                         the edges whose interval can still hold a minimum), elder-rule
+//                         salience, top-k CSR (see the section comment below)
+// This part runs binary64 at a small fraction of its binary32 rate, so the nb^2 x D binary64
+// distance matrix would cost more than all other schedule work together; Boruvka needs the
+// exact key only to decide between edges whose intervals overlap the smallest upper bound.
 #include <climits>
 
 #include "tsa_device.cuh"
@@ -348,8 +354,19 @@ __device__ __forceinline__ void hold8(double *v) {
     asm volatile("" : "+d"(v[0]), "+d"(v[1]), "+d"(v[2]), "+d"(v[3]), "+d"(v[4]), "+d"(v[5]), "+d"(v[6]), "+d"(v[7]));
 }
 
+// Binary32 copy of a centroid coordinate for the distance bounds.  Zero and magnitudes in
+// [2^-60, 2^60] round to nearest as normal binary32 numbers (relative error <= 2^-24, and
+// every difference of two of them is a normal number or zero); anything else becomes NaN,
+// which makes every bound of that block's pairs the whole range [0, +inf].
+__device__ __forceinline__ float bounds_copy(double x) {
+    const double m = fabs(x);
+    if (x == 0.0) return 0.0f;
+    return (m >= 0x1p-60 && m <= 0x1p60) ? __double2float_rn(x) : __int_as_float(0x7fc00000);
+}
+
 __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, int64_t nb,
-                               int64_t D, int64_t S, int64_t block, double *__restrict__ C) {
+                               int64_t D, int64_t S, int64_t block, double *__restrict__ C,
+                               float *__restrict__ C32) {
     const int64_t n = nb * D;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n;
          w += (int64_t)gridDim.x * blockDim.x) {
@@ -368,7 +385,9 @@ __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, i
             for (int i = 0; i < 16; ++i) total += v[i];
         }
         for (; l < lanes; ++l) total += part[l * n + w];
-        C[w] = total / (double)(n_b * lanes);
+        const double c = total / (double)(n_b * lanes);
+        C[w] = c;
+        C32[w] = bounds_copy(c);
     }
 }
 
@@ -410,79 +429,124 @@ __global__ void content_rank(const double *__restrict__ C, int64_t nb, int64_t D
     if (lane == 0) perm[count] = (int)b;
 }
 
-// Cp[r][:] = C[perm[r]][:]
+// Cp[r][:] = C[perm[r]][:], and its binary32 copy
 __global__ void permute_rows(const double *__restrict__ C, const int *__restrict__ perm, int64_t nb,
-                             int64_t D, double *__restrict__ Cp) {
+                             int64_t D, double *__restrict__ Cp, float *__restrict__ Cp32) {
     const int64_t n = nb * D;
     for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < n;
          w += (int64_t)gridDim.x * blockDim.x)
     {
         const int b = perm[w / D];
-        Cp[w] = (b >= 0 && b < nb) ? C[(int64_t)b * D + w % D] : 0.0;
+        const double c = (b >= 0 && b < nb) ? C[(int64_t)b * D + w % D] : 0.0;
+        Cp[w] = c;
+        Cp32[w] = bounds_copy(c);
     }
 }
 
-// ---------------------------------------------------------------- pairwise distances
-constexpr int kPdTile = 16;   // pairs per tile side
-constexpr int kPdChunk = 32;  // d values staged per step
-constexpr int kPdFlatBelow = 256;  // nb below which pairwise_d2_flat runs instead
+// ---------------------------------------------------------------- distance bounds
+constexpr int kPbTile = 16;        // pairs per tile side
+constexpr int kPbChunk = 32;       // d values staged per step
+constexpr int kPbFlatBelow = 256;  // nb below which pairwise_bounds_flat runs instead
 
-// D2[u][v] = D2[v][u] = sum_{d ascending} fma(C[u][d]-C[v][d], same, acc).  One CTA per tile
-// (tu <= tv) of the upper triangle, 64 threads, 2 x 2 pairs each.  (C[v]-C[u] is exactly
-// -(C[u]-C[v]), so the mirrored entry is bit-identical to computing it directly.)
-__global__ void __launch_bounds__(64) pairwise_d2(const double *__restrict__ C, int64_t nb,
-                                                  int64_t D, int tiles, double *__restrict__ D2) {
-    __shared__ double cu[kPdTile][kPdChunk + 1];
-    __shared__ double cv[kPdTile][kPdChunk + 1];
+// An interval [lo, hi] that holds the binary64 squared distance the graph kernel (and the
+// oracle) computes from (C_u[d] - C_v[d])^2 (exact_d2 below), given
+//   s       the binary32 fma-chain sum of (a_d - b_d)^2, a and b the rows' binary32 copies;
+//   na, nv  the binary32 fma-chain sums of a_d^2 and b_d^2;
+//   rel     D * 2^-22 (D <= 1024).
+// Error budget; every step below rounds outward, so the interval can only widen:
+//   * |a_d - C_u[d]| <= 2^-24 |C_u[d]| (normal binary32 range, see bounds_copy) and the
+//     binary32 subtraction adds at most 2^-24 |a_d - b_d|, so each difference is off from the
+//     exact C_u[d] - C_v[d] by e_d <= 2^-22 (|a_d| + |b_d|);
+//   * hence the exact sum of (a_d - b_d)^2 (the terms s rounds) is off from the exact
+//     sum of (C_u[d] - C_v[d])^2 by at most sum e_d (2 |a_d - b_d| + e_d)
+//     <= 2^-21 sqrt(N) sqrt(s*) + 2^-44 N, with N = 2 (sum a^2 + sum b^2) >= sum (|a|+|b|)^2
+//     (Cauchy-Schwarz) and s* that exact sum of squares;
+//   * a binary32 recursive sum of D non-negative terms is within a factor 1 -+ D 2^-23 of its
+//     exact value, plus at most D 2^-149 from terms that underflow (inside the 2^-120 slack);
+//   * the binary64 sum rounds each term at most D / 32 + 8 times, so it is within a factor
+//     1 -+ (D + 8) 2^-53 of the exact real sum, inside
+//     the final factor 1 -+ 2^-20; no binary64 step under- or overflows for coordinates in
+//     bounds_copy's range.
+// NaN anywhere (a block outside that range) or a binary32 overflow gives [0, +inf].
+__device__ __forceinline__ float2 d2_interval(float s, float na, float nv, float rel) {
+    const float tiny = 0x1p-120f;
+    const float up = 1.0f + rel, dn = 1.0f - rel;  // exact: rel is a multiple of 2^-22, <= 2^-12
+    const float s_up = __fmul_ru(__fadd_ru(s, tiny), up);
+    const float s_dn = __fmul_rd(__fsub_rd(s, tiny), dn);
+    const float n_up = __fmul_ru(__fmul_ru(__fadd_ru(__fadd_ru(na, nv), tiny), up), 2.0f);
+    const float e = __fmaf_ru(0x1p-21f, __fmul_ru(__fsqrt_ru(n_up), __fsqrt_ru(s_up)), __fmul_ru(0x1p-44f, n_up));
+    float hi = __fmul_ru(__fadd_ru(s_up, e), 1.0f + 0x1p-20f);
+    float lo = __fmul_rd(__fsub_rd(s_dn, e), 1.0f - 0x1p-20f);
+    hi = hi <= 0x1.fffffep127f ? hi : __int_as_float(0x7f800000);  // NaN or overflow: +inf
+    lo = lo > 0.0f ? lo : 0.0f;                                      // NaN or negative: 0
+    return make_float2(lo, hi);
+}
+
+// B[u][v] = B[v][u] = the interval of d2(u, v).  One CTA per tile (tu <= tv) of the upper
+// triangle, 64 threads, 2 x 2 pairs each; the CTA's 32 rows get their squared norms from the
+// same staged values (threads 0..31, one row each).  The binary32 arithmetic is symmetric in
+// u and v, so the mirrored entry is the interval computed for (v, u).
+__global__ void __launch_bounds__(64) pairwise_bounds(const float *__restrict__ C, int64_t nb, int64_t D,
+                                                      int tiles, float rel, float2 *__restrict__ B) {
+    __shared__ float cu[kPbTile][kPbChunk + 1];
+    __shared__ float cv[kPbTile][kPbChunk + 1];
+    __shared__ float nrm[2 * kPbTile];
     // linear tile index -> (tu, tv), tu <= tv, row-major over the upper triangle
     int k = blockIdx.x, tu = 0;
     while (k >= tiles - tu) { k -= tiles - tu; ++tu; }
     const int tv = tu + k;
-    const int tx = threadIdx.x & 7, ty = threadIdx.x >> 3;
-    const int64_t u0 = (int64_t)tu * kPdTile, v0 = (int64_t)tv * kPdTile;
-    double acc[2][2] = {{0.0, 0.0}, {0.0, 0.0}};
-    for (int64_t d0 = 0; d0 < D; d0 += kPdChunk) {
-        for (int i = threadIdx.x; i < kPdTile * kPdChunk; i += 64) {
-            const int r = i / kPdChunk, c = i % kPdChunk;
+    const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
+    const int64_t u0 = (int64_t)tu * kPbTile, v0 = (int64_t)tv * kPbTile;
+    float acc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+    float nacc = 0.0f;
+    for (int64_t d0 = 0; d0 < D; d0 += kPbChunk) {
+        for (int i = tid; i < kPbTile * kPbChunk; i += 64) {
+            const int r = i / kPbChunk, c = i % kPbChunk;
             const int64_t d = d0 + c;
-            cu[r][c] = (u0 + r < nb && d < D) ? C[(u0 + r) * D + d] : 0.0;
-            cv[r][c] = (v0 + r < nb && d < D) ? C[(v0 + r) * D + d] : 0.0;
+            cu[r][c] = (u0 + r < nb && d < D) ? C[(u0 + r) * D + d] : 0.0f;
+            cv[r][c] = (v0 + r < nb && d < D) ? C[(v0 + r) * D + d] : 0.0f;
         }
         __syncthreads();
-        const int dn = (int)((D - d0) < kPdChunk ? (D - d0) : kPdChunk);
+        const int dn = (int)((D - d0) < kPbChunk ? (D - d0) : kPbChunk);
+        if (tid < 2 * kPbTile) {
+            const float *row = tid < kPbTile ? cu[tid] : cv[tid - kPbTile];
+            for (int c = 0; c < dn; ++c) nacc = __fmaf_rn(row[c], row[c], nacc);
+        }
 #pragma unroll 4
         for (int c = 0; c < dn; ++c) {
-            const double a0 = cu[ty * 2][c], a1 = cu[ty * 2 + 1][c];
-            const double b0 = cv[tx * 2][c], b1 = cv[tx * 2 + 1][c];
-            double t;
-            t = a0 - b0; acc[0][0] = fma(t, t, acc[0][0]);
-            t = a0 - b1; acc[0][1] = fma(t, t, acc[0][1]);
-            t = a1 - b0; acc[1][0] = fma(t, t, acc[1][0]);
-            t = a1 - b1; acc[1][1] = fma(t, t, acc[1][1]);
+            const float a0 = cu[ty * 2][c], a1 = cu[ty * 2 + 1][c];
+            const float b0 = cv[tx * 2][c], b1 = cv[tx * 2 + 1][c];
+            float t;
+            t = __fsub_rn(a0, b0); acc[0][0] = __fmaf_rn(t, t, acc[0][0]);
+            t = __fsub_rn(a0, b1); acc[0][1] = __fmaf_rn(t, t, acc[0][1]);
+            t = __fsub_rn(a1, b0); acc[1][0] = __fmaf_rn(t, t, acc[1][0]);
+            t = __fsub_rn(a1, b1); acc[1][1] = __fmaf_rn(t, t, acc[1][1]);
         }
         __syncthreads();
     }
+    if (tid < 2 * kPbTile) nrm[tid] = nacc;
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < 2; ++i)
 #pragma unroll
         for (int k2 = 0; k2 < 2; ++k2) {
             const int64_t u = u0 + ty * 2 + i, v = v0 + tx * 2 + k2;
             if (u < nb && v < nb) {
-                D2[u * nb + v] = acc[i][k2];
-                D2[v * nb + u] = acc[i][k2];
+                const float2 iv = d2_interval(acc[i][k2], nrm[ty * 2 + i], nrm[kPbTile + tx * 2 + k2], rel);
+                B[u * nb + v] = iv;
+                B[v * nb + u] = iv;
             }
         }
 }
 
-// The same distances for small nb, where the tiled kernel would run a handful of CTAs (one
-// at nb = 16): one thread per pair u < v, 32 pairs per CTA, so the FP64 chains spread over
-// as many SMs as there are warps.  The diagonal is written as +0, like the tiled kernel's
-// fma(0, 0, 0).
-__global__ void __launch_bounds__(32) pairwise_d2_flat(const double *__restrict__ C, int64_t nb, int64_t D,
-                                                       double *__restrict__ D2) {
+// The same intervals for small nb, where the tiled kernel would run a handful of CTAs: one
+// thread per pair u < v, 32 pairs per CTA.  The diagonal gets [0, 0] (a block is never an edge
+// of its own component).
+__global__ void __launch_bounds__(32) pairwise_bounds_flat(const float *__restrict__ C, int64_t nb, int64_t D,
+                                                           float rel, float2 *__restrict__ B) {
     const int64_t npairs = nb * (nb - 1) / 2;
     const int64_t p = (int64_t)blockIdx.x * 32 + threadIdx.x;
-    if (p < nb) D2[p * nb + p] = 0.0;
+    if (p < nb) B[p * nb + p] = make_float2(0.0f, 0.0f);
     if (p >= npairs) return;
     // p -> (u, v), u < v, row-major over the strict upper triangle: row u starts at
     // u * (2 nb - u - 1) / 2.  Float estimate, then exact integer correction.
@@ -493,34 +557,34 @@ __global__ void __launch_bounds__(32) pairwise_d2_flat(const double *__restrict_
     while (u > 0 && u * (2 * nb - u - 1) / 2 > p) --u;
     while ((u + 1) * (2 * nb - u - 2) / 2 <= p) ++u;
     const int64_t v = u + 1 + (p - u * (2 * nb - u - 1) / 2);
-    const double *cu = C + u * D, *cv = C + v * D;
-    // d ascending; the loads of 32 d are issued before their fma chain
-    double acc = 0.0;
+    const float *cu = C + u * D, *cv = C + v * D;
+    float s = 0.0f, na = 0.0f, nv = 0.0f;
     int64_t d = 0;
-    for (; d + 32 <= D; d += 32) {
-        double a[32], b[32];
+    for (; d + 16 <= D; d += 16) {
+        float a[16], b[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
             a[i] = __ldg(cu + d + i);
             b[i] = __ldg(cv + d + i);
         }
 #pragma unroll
-        for (int i = 0; i < 32; i += 8) {
-            hold8(a + i);
-            hold8(b + i);
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const double t = a[i] - b[i];
-            acc = fma(t, t, acc);
+        for (int i = 0; i < 16; ++i) {
+            const float t = __fsub_rn(a[i], b[i]);
+            s = __fmaf_rn(t, t, s);
+            na = __fmaf_rn(a[i], a[i], na);
+            nv = __fmaf_rn(b[i], b[i], nv);
         }
     }
     for (; d < D; ++d) {
-        const double t = __ldg(cu + d) - __ldg(cv + d);
-        acc = fma(t, t, acc);
+        const float a = __ldg(cu + d), b = __ldg(cv + d);
+        const float t = __fsub_rn(a, b);
+        s = __fmaf_rn(t, t, s);
+        na = __fmaf_rn(a, a, na);
+        nv = __fmaf_rn(b, b, nv);
     }
-    D2[u * nb + v] = acc;
-    D2[v * nb + u] = acc;
+    const float2 iv = d2_interval(s, na, nv, rel);
+    B[u * nb + v] = iv;
+    B[v * nb + u] = iv;
 }
 
 // ---------------------------------------------------------------- MST, elder rule, CSR
@@ -528,7 +592,11 @@ __global__ void __launch_bounds__(32) pairwise_d2_flat(const double *__restrict_
 // resident (cudaLaunchCooperativeKernel), so they can meet at grid-wide barriers; the barrier
 // is bounded in time like every other wait here.
 //   Boruvka rounds: all warps find each vertex's lightest edge to another component (strict
-//     key (d2, min(u,v), max(u,v))); CTA 0 takes each component's lightest edge, hooks along
+//     key (d2, min(u,v), max(u,v))): the smallest upper bound H over its edges to other
+//     components, then the exact binary64 d2 of every such edge whose lower bound is <= H (the
+//     lightest edge is among them); a vertex whose previous lightest edge still leaves its
+//     component keeps it (its edge set only shrinks).  CTA 0 takes each component's lightest
+//     edge, hooks along
 //     it (a mutual pair keeps the smaller label as root), records each chosen edge once,
 //     flattens by pointer jumping and relabels.  The rounds stop at one component.
 //   Elder rule (CTA 0): bitonic sort of the nb-1 MST edges by the same key, then one warp
@@ -539,7 +607,9 @@ __global__ void __launch_bounds__(32) pairwise_d2_flat(const double *__restrict_
 //     blocks from a per-row bitmap (sink range, local window, first topk blocks <= i of the
 //     order); CTA 0 scans the counts into row_ptr; warps fill col_idx in ascending order.
 struct GraphArgs {
-    const double *d2;
+    const float2 *bnd;  // [nb][nb] intervals [lo, hi] holding the binary64 d2
+    const double *cent; // [nb][D] centroids (in rank order under the content rule)
+    int64_t D;
     int nb, pow2, sink, r, topk, rounds;
     size_t xs_offset;  // byte offset of the sort exchange buffer in dynamic shared memory
     int *comp;
@@ -603,42 +673,111 @@ __device__ __forceinline__ bool key_less(double d1, int a1, int b1, double d2, i
     return b1 < b2;
 }
 
+// The exact binary64 d2 of blocks x and y in the fixed order of summation: lane j accumulates
+// the terms d = j, j + 32, ... (ascending, one fused multiply-add each, from +0) of
+// t_d = C[x][d] - C[y][d] (the square of -t is the square of t, so the sign does not matter),
+// then halving adds: after the step with offset w every lane holds P_(j mod w) + P_(j mod w + w)
+// (the two lanes of a pair add the same two values, and binary64 addition is commutative).
+// A dependent binary64 operation takes a few hundred cycles here, so this is ~4 chain steps and
+// 5 additions for D = 128 instead of 128 steps.
+__device__ __forceinline__ double exact_d2(const double *__restrict__ C, int64_t D, int x, int y, int lane) {
+    const double *cx = C + (int64_t)x * D, *cy = C + (int64_t)y * D;
+    double acc = 0.0;
+    int64_t d = lane;
+    for (; d + 96 < D; d += 128) {  // four terms per lane in flight
+        const double a0 = __ldg(cx + d), b0 = __ldg(cy + d);
+        const double a1 = __ldg(cx + d + 32), b1 = __ldg(cy + d + 32);
+        const double a2 = __ldg(cx + d + 64), b2 = __ldg(cy + d + 64);
+        const double a3 = __ldg(cx + d + 96), b3 = __ldg(cy + d + 96);
+        double t;
+        t = a0 - b0; acc = fma(t, t, acc);
+        t = a1 - b1; acc = fma(t, t, acc);
+        t = a2 - b2; acc = fma(t, t, acc);
+        t = a3 - b3; acc = fma(t, t, acc);
+    }
+    for (; d < D; d += 32) {
+        const double t = __ldg(cx + d) - __ldg(cy + d);
+        acc = fma(t, t, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, off);
+    return acc;
+}
+
 // Each vertex's lightest edge to another component; one warp per vertex, grid-wide.  Every
-// CTA keeps its own copy of the component labels in shared memory (`scomp`); each lane reads
-// its d2 entries in independent batches of 16 (one batch covers a 512-block row).
-__device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, double *vb_d, int *vb_u) {
+// CTA keeps its own copy of the component labels in shared memory (`scomp`).  Round 0 and
+// every vertex whose previous lightest edge now stays inside its component scan the row of
+// intervals: H = the smallest upper bound over edges to other components, then the exact key
+// of each such edge with lower bound <= H.  The edge of least exact d2 has lower bound <= its
+// d2 <= H, so it is always among them.  Equal d2 go to the smaller (min, max) pair.
+__device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, int round) {
     const int nb = a.nb;
     const int lane = threadIdx.x & 31;
     const int wpb = blockDim.x >> 5;
     const int total = gridDim.x * wpb;
+    double *vb_d = a.vb_d + (round & 1) * nb;
+    int *vb_u = a.vb_u + (round & 1) * nb;
+    const double *pvb_d = a.vb_d + ((round + 1) & 1) * nb;
+    const int *pvb_u = a.vb_u + ((round + 1) & 1) * nb;
     for (int v = blockIdx.x * wpb + (threadIdx.x >> 5); v < nb; v += total) {
         const int cv = scomp[v];
-        double bd = __longlong_as_double((long long)kInfBits);
-        int ba = INT_MAX, bb = INT_MAX, bu = -1;
-        const double *row = a.d2 + (int64_t)v * nb;
-        for (int u0 = lane; u0 < nb; u0 += 32 * 16) {
-            double d[16];
+        if (round > 0) {
+            // written by some warp of the previous round, before the grid barrier
+            const int pu = __ldcg(pvb_u + v);
+            if (pu >= 0 && scomp[pu] != cv) {
+                if (lane == 0) {
+                    vb_d[v] = __ldcg(pvb_d + v);
+                    vb_u[v] = pu;
+                }
+                continue;
+            }
+        }
+        const float2 *row = a.bnd + (int64_t)v * nb;
+        float h = __int_as_float(0x7f800000);
+        for (int base = 0; base < nb; base += 32 * 16) {
+            float hi[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const int u = u0 + 32 * k;
-                d[k] = u < nb ? __ldg(row + u) : 0.0;
+                const int u = base + lane + 32 * k;
+                hi[k] = u < nb ? __ldg(&row[u].y) : 0.0f;
             }
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const int u = u0 + 32 * k;
-                if (u < nb && scomp[u] != cv) {
-                    const int x = u < v ? u : v, y = u < v ? v : u;
-                    if (key_less(d[k], x, y, bd, ba, bb)) { bd = d[k]; ba = x; bb = y; bu = u; }
-                }
+                const int u = base + lane + 32 * k;
+                if (u < nb && scomp[u] != cv) h = fminf(h, hi[k]);
             }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const double od = __shfl_xor_sync(0xffffffffu, bd, off);
-            const int oa = __shfl_xor_sync(0xffffffffu, ba, off);
-            const int ob = __shfl_xor_sync(0xffffffffu, bb, off);
-            const int ou = __shfl_xor_sync(0xffffffffu, bu, off);
-            if (key_less(od, oa, ob, bd, ba, bb)) { bd = od; ba = oa; bb = ob; bu = ou; }
+        for (int off = 16; off > 0; off >>= 1) h = fminf(h, __shfl_xor_sync(0xffffffffu, h, off));
+        // the exact keys of the candidates, warp-uniform
+        double bd = __longlong_as_double((long long)kInfBits);
+        int ba = INT_MAX, bb = INT_MAX, bu = -1;
+        for (int base = 0; base < nb; base += 32 * 16) {
+            float lo[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int u = base + lane + 32 * k;
+                lo[k] = u < nb ? __ldg(&row[u].x) : 0.0f;
+            }
+            // lane k keeps the candidate mask of batch slot k
+            unsigned mine = 0u;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const int u = base + lane + 32 * k;
+                const unsigned m = __ballot_sync(0xffffffffu, u < nb && scomp[u] != cv && lo[k] <= h);
+                if (lane == k) mine = m;
+            }
+#pragma unroll 1
+            for (int k = 0; k < 16; ++k) {
+                unsigned m = __shfl_sync(0xffffffffu, mine, k);
+                while (m != 0u) {
+                    const int w = base + (__ffs((int)m) - 1) + 32 * k;
+                    m &= m - 1u;
+                    const double d = exact_d2(a.cent, a.D, v, w, lane);
+                    const int x = w < v ? w : v, y = w < v ? v : w;
+                    if (key_less(d, x, y, bd, ba, bb)) { bd = d; ba = x; bb = y; bu = w; }
+                }
+            }
         }
         if (lane == 0) {
             vb_d[v] = bd;
@@ -947,7 +1086,7 @@ __device__ void row_bitmap(const int *order, unsigned *bm, int words, int nb, in
     __syncwarp();
 }
 
-__global__ void __launch_bounds__(512) schedule_graph_kernel(GraphArgs a) {
+__global__ void __launch_bounds__(512, 1) schedule_graph_kernel(GraphArgs a) {
     extern __shared__ __align__(16) uint8_t sm[];
     const int nb = a.nb;
     const int tid = threadIdx.x, nt = blockDim.x;
@@ -962,11 +1101,9 @@ __global__ void __launch_bounds__(512) schedule_graph_kernel(GraphArgs a) {
     __syncthreads();
     int ncomp = nb, n_edges = 0;
     for (int round = 0; round < a.rounds && ncomp > 1; ++round) {
-        double *vb_d = a.vb_d + (round & 1) * nb;
-        int *vb_u = a.vb_u + (round & 1) * nb;
-        vertex_min_phase(a, scomp, vb_d, vb_u);
+        vertex_min_phase(a, scomp, round);
         if (!grid_sync(a.gbar, a.flags)) return;
-        ncomp = merge_phase(a, sm, scomp, vb_d, vb_u, &n_edges);
+        ncomp = merge_phase(a, sm, scomp, a.vb_d + (round & 1) * nb, a.vb_u + (round & 1) * nb, &n_edges);
     }
     // ---- elder rule (CTA 0 holds the MST edges it recorded)
     if (blockIdx.x == 0) elder_phase(a, sm, n_edges, xs);
@@ -1118,7 +1255,8 @@ ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D
     };
     w.part = take(sizeof(double) * (size_t)(lanes * nb * D));
     w.cent = take(sizeof(double) * (size_t)(nb * D));
-    w.d2 = take(sizeof(double) * (size_t)(nb * nb));
+    w.cent32 = take(sizeof(float) * (size_t)(nb * D));
+    w.bnd = take(sizeof(float2) * (size_t)(nb * nb));
     w.comp = take(sizeof(int) * (size_t)nb);
     w.vb_d = take(sizeof(double) * (size_t)(2 * nb));
     w.vb_u = take(sizeof(int) * (size_t)(2 * nb));
@@ -1184,7 +1322,8 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     uint8_t *w = a.workspace;
     double *part = reinterpret_cast<double *>(w + ws.part);
     double *cent = reinterpret_cast<double *>(w + ws.cent);
-    double *d2 = reinterpret_cast<double *>(w + ws.d2);
+    float *cent32 = reinterpret_cast<float *>(w + ws.cent32);
+    float2 *bnd = reinterpret_cast<float2 *>(w + ws.bnd);
     int *comp = reinterpret_cast<int *>(w + ws.comp);
     double *vb_d = reinterpret_cast<double *>(w + ws.vb_d);
     int *vb_u = reinterpret_cast<int *>(w + ws.vb_u);
@@ -1199,7 +1338,7 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     {
         const int64_t n = a.nb * a.D;
         const unsigned g = (unsigned)((n + 255) / 256);
-        centroid_final<<<g, 256, 0, st>>>(sums, a.lanes, a.nb, a.D, a.S, a.block, cent);
+        centroid_final<<<g, 256, 0, st>>>(sums, a.lanes, a.nb, a.D, a.S, a.block, cent, cent32);
     }
     // content rule: rank the blocks, run the graph on the centroids in rank order
     int *perm = nullptr;
@@ -1209,17 +1348,18 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
         content_rank<<<(unsigned)((a.nb + 7) / 8), 256, 0, st>>>(cent, a.nb, a.D, perm);
         const int64_t n = a.nb * a.D;
         permute_rows<<<(unsigned)((n + 255) / 256 < 152 * 16 ? (n + 255) / 256 : 152 * 16), 256, 0, st>>>(
-            cent, perm, a.nb, a.D, part);
+            cent, perm, a.nb, a.D, part, cent32);
         graph_cent = part;  // the workspace's block-sum area; centroid_final has read the sums
     }
-    // distances
-    if (nb < kPdFlatBelow) {
+    // distance intervals (D <= 1024, so rel = D * 2^-22 is exact and at most 2^-12)
+    const float rel = ldexpf((float)a.D, -22);
+    if (nb < kPbFlatBelow) {
         const int64_t npairs = a.nb * (a.nb - 1) / 2;
         const int64_t n = npairs > a.nb ? npairs : a.nb;
-        pairwise_d2_flat<<<(unsigned)((n + 31) / 32), 32, 0, st>>>(graph_cent, a.nb, a.D, d2);
+        pairwise_bounds_flat<<<(unsigned)((n + 31) / 32), 32, 0, st>>>(cent32, a.nb, a.D, rel, bnd);
     } else {
-        const int t = (nb + kPdTile - 1) / kPdTile;
-        pairwise_d2<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(graph_cent, a.nb, a.D, t, d2);
+        const int t = (nb + kPbTile - 1) / kPbTile;
+        pairwise_bounds<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(cent32, a.nb, a.D, t, rel, bnd);
     }
     // MST, elder rule and CSR in one cooperative launch
     int rounds = 0;
@@ -1250,7 +1390,9 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     unsigned *gbar = reinterpret_cast<unsigned *>(w + ws.gbar);
     if (cudaMemsetAsync(gbar, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return TSA_ERR_CUDA;
     GraphArgs g;
-    g.d2 = d2;
+    g.bnd = bnd;
+    g.cent = graph_cent;
+    g.D = a.D;
     g.nb = nb;
     g.pow2 = pow2;
     g.sink = (int)a.sink;

@@ -79,7 +79,7 @@ constexpr int64_t kMaxScheduleDim = 1024;
 
 // Byte offsets of the builder's workspace regions (each 256-byte aligned).
 struct ScheduleWorkspace {
-    size_t part, cent, d2, comp, vb_d, vb_u, mst_d, mst_u, mst_v, counters, sal, cnt, perm, sal_rank, gbar, total;
+    size_t part, cent, cent32, bnd, comp, vb_d, vb_u, mst_d, mst_u, mst_v, counters, sal, cnt, perm, sal_rank, gbar, total;
 };
 ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D);
 
