@@ -483,11 +483,13 @@ __device__ __forceinline__ float2 d2_interval(float s, float na, float nv, float
 }
 
 // B[u][v] = B[v][u] = the interval of d2(u, v).  One CTA per tile (tu <= tv) of the upper
-// triangle, 64 threads, 2 x 2 pairs each; the CTA's 32 rows get their squared norms from the
-// same staged values (threads 0..31, one row each).  The binary32 arithmetic is symmetric in
-// u and v, so the mirrored entry is the interval computed for (v, u).
-__global__ void __launch_bounds__(64) pairwise_bounds(const float *__restrict__ C, int64_t nb, int64_t D,
-                                                      int tiles, float rel, float2 *__restrict__ B) {
+// triangle, 256 threads, one pair each (many resident warps hide the staging loads); the
+// tile's 32 rows get their squared norms from the same staged values (threads 0..31, one row
+// each).  The binary32 arithmetic is symmetric in u and v, so the mirrored entry is the
+// interval computed for (v, u).
+constexpr int kPbThreads = kPbTile * kPbTile;
+__global__ void __launch_bounds__(kPbThreads) pairwise_bounds(const float *__restrict__ C, int64_t nb, int64_t D,
+                                                              int tiles, float rel, float2 *__restrict__ B) {
     __shared__ float cu[kPbTile][kPbChunk + 1];
     __shared__ float cv[kPbTile][kPbChunk + 1];
     __shared__ float nrm[2 * kPbTile];
@@ -495,12 +497,11 @@ __global__ void __launch_bounds__(64) pairwise_bounds(const float *__restrict__ 
     int k = blockIdx.x, tu = 0;
     while (k >= tiles - tu) { k -= tiles - tu; ++tu; }
     const int tv = tu + k;
-    const int tid = threadIdx.x, tx = tid & 7, ty = tid >> 3;
+    const int tid = threadIdx.x, tx = tid % kPbTile, ty = tid / kPbTile;
     const int64_t u0 = (int64_t)tu * kPbTile, v0 = (int64_t)tv * kPbTile;
-    float acc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
-    float nacc = 0.0f;
+    float acc = 0.0f, nacc = 0.0f;
     for (int64_t d0 = 0; d0 < D; d0 += kPbChunk) {
-        for (int i = tid; i < kPbTile * kPbChunk; i += 64) {
+        for (int i = tid; i < kPbTile * kPbChunk; i += kPbThreads) {
             const int r = i / kPbChunk, c = i % kPbChunk;
             const int64_t d = d0 + c;
             cu[r][c] = (u0 + r < nb && d < D) ? C[(u0 + r) * D + d] : 0.0f;
@@ -512,31 +513,21 @@ __global__ void __launch_bounds__(64) pairwise_bounds(const float *__restrict__ 
             const float *row = tid < kPbTile ? cu[tid] : cv[tid - kPbTile];
             for (int c = 0; c < dn; ++c) nacc = __fmaf_rn(row[c], row[c], nacc);
         }
-#pragma unroll 4
+#pragma unroll 8
         for (int c = 0; c < dn; ++c) {
-            const float a0 = cu[ty * 2][c], a1 = cu[ty * 2 + 1][c];
-            const float b0 = cv[tx * 2][c], b1 = cv[tx * 2 + 1][c];
-            float t;
-            t = __fsub_rn(a0, b0); acc[0][0] = __fmaf_rn(t, t, acc[0][0]);
-            t = __fsub_rn(a0, b1); acc[0][1] = __fmaf_rn(t, t, acc[0][1]);
-            t = __fsub_rn(a1, b0); acc[1][0] = __fmaf_rn(t, t, acc[1][0]);
-            t = __fsub_rn(a1, b1); acc[1][1] = __fmaf_rn(t, t, acc[1][1]);
+            const float t = __fsub_rn(cu[ty][c], cv[tx][c]);
+            acc = __fmaf_rn(t, t, acc);
         }
         __syncthreads();
     }
     if (tid < 2 * kPbTile) nrm[tid] = nacc;
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int k2 = 0; k2 < 2; ++k2) {
-            const int64_t u = u0 + ty * 2 + i, v = v0 + tx * 2 + k2;
-            if (u < nb && v < nb) {
-                const float2 iv = d2_interval(acc[i][k2], nrm[ty * 2 + i], nrm[kPbTile + tx * 2 + k2], rel);
-                B[u * nb + v] = iv;
-                B[v * nb + u] = iv;
-            }
-        }
+    const int64_t u = u0 + ty, v = v0 + tx;
+    if (u < nb && v < nb) {
+        const float2 iv = d2_interval(acc, nrm[ty], nrm[kPbTile + tx], rel);
+        B[u * nb + v] = iv;
+        B[v * nb + u] = iv;
+    }
 }
 
 // The same intervals for small nb, where the tiled kernel would run a handful of CTAs: one
@@ -1359,7 +1350,7 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
         pairwise_bounds_flat<<<(unsigned)((n + 31) / 32), 32, 0, st>>>(cent32, a.nb, a.D, rel, bnd);
     } else {
         const int t = (nb + kPbTile - 1) / kPbTile;
-        pairwise_bounds<<<(unsigned)(t * (t + 1) / 2), 64, 0, st>>>(cent32, a.nb, a.D, t, rel, bnd);
+        pairwise_bounds<<<(unsigned)(t * (t + 1) / 2), kPbThreads, 0, st>>>(cent32, a.nb, a.D, t, rel, bnd);
     }
     // MST, elder rule and CSR in one cooperative launch
     int rounds = 0;
