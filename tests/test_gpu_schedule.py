@@ -130,6 +130,21 @@ def test_distances_below_binary32_resolution(nb, dtype, jmax):
     _assert_same(_gpu_schedule(kd, block, 1, 2, 4), _oracle_schedule(kd, block, 1, 2, 4), distinct=False)
 
 
+@pytest.mark.parametrize("spread", [0, 16, 24, 60])
+def test_lane_sum_integer_path_and_fallback(spread):
+    """Lane means over 5 lanes whose keys differ in scale by up to 2^spread.  At 0 and 16 the
+    block sums of all lanes fit 53 bits at their common lowest bit in every column, so the lane
+    sum is exact and the GPU adds integers; at 24 about a quarter of the columns do (a mix of
+    both paths in one launch); at 60 none do and it adds in binary64 lane by lane.  Either way
+    the CSR and the salience equal the oracle's bit for bit."""
+    g = torch.Generator().manual_seed(100 + spread)
+    lanes, nb, D = 5, 20, 8
+    x = torch.randn((lanes, nb * 64, D), generator=g)
+    x = x * torch.pow(2.0, torch.tensor([0.0, spread, -spread / 2, spread / 3, 1.0])).view(lanes, 1, 1)
+    k = x.to(torch.bfloat16).to(DEV)
+    _assert_same(_gpu_schedule(k, 64, 1, 2, 3), _oracle_schedule(k, 64, 1, 2, 3))
+
+
 def test_largest_block_count():
     nb = 4096
     gen = torch.Generator().manual_seed(7)

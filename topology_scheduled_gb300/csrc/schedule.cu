@@ -385,7 +385,16 @@ __global__ void centroid_final(const double *__restrict__ part, int64_t lanes, i
             for (int i = 0; i < 16; ++i) total += v[i];
         }
         for (; l < lanes; ++l) total += part[l * n + w];
-        const double c = total / (double)(n_b * lanes);
+        // A power-of-two divisor 2^k: multiplying by the exact 2^-k rounds the same exact
+        // quotient as the division, without the binary64 divide's instruction sequence.
+        const int64_t N = n_b * lanes;
+        double c;
+        if ((N & (N - 1)) == 0) {
+            const int k = 63 - __clzll((long long)N);
+            c = total * __longlong_as_double((long long)(1023 - k) << 52);
+        } else {
+            c = total / (double)N;
+        }
         C[w] = c;
         C32[w] = bounds_copy(c);
     }
@@ -485,13 +494,16 @@ __device__ __forceinline__ float2 d2_interval(float s, float na, float nv, float
 // B[u][v] = B[v][u] = the interval of d2(u, v).  One CTA per tile (tu <= tv) of the upper
 // triangle, 256 threads, one pair each (many resident warps hide the staging loads); the
 // tile's 32 rows get their squared norms from the same staged values (threads 0..31, one row
-// each).  The binary32 arithmetic is symmetric in u and v, so the mirrored entry is the
-// interval computed for (v, u).
+// each).  Chunks are zero-padded past D (a zero difference adds exactly nothing), and rows are
+// 16-byte aligned in shared memory so that each thread reads four coordinates per load.  The
+// binary32 arithmetic is symmetric in u and v, so the mirrored entry is the interval computed
+// for (v, u).
 constexpr int kPbThreads = kPbTile * kPbTile;
+constexpr int kPbPitch = kPbChunk + 4;  // floats per staged row: 16-byte rows, no bank conflicts
 __global__ void __launch_bounds__(kPbThreads) pairwise_bounds(const float *__restrict__ C, int64_t nb, int64_t D,
                                                               int tiles, float rel, float2 *__restrict__ B) {
-    __shared__ float cu[kPbTile][kPbChunk + 1];
-    __shared__ float cv[kPbTile][kPbChunk + 1];
+    __shared__ __align__(16) float cu[kPbTile][kPbPitch];
+    __shared__ __align__(16) float cv[kPbTile][kPbPitch];
     __shared__ float nrm[2 * kPbTile];
     // linear tile index -> (tu, tv), tu <= tv, row-major over the upper triangle
     int k = blockIdx.x, tu = 0;
@@ -508,15 +520,26 @@ __global__ void __launch_bounds__(kPbThreads) pairwise_bounds(const float *__res
             cv[r][c] = (v0 + r < nb && d < D) ? C[(v0 + r) * D + d] : 0.0f;
         }
         __syncthreads();
-        const int dn = (int)((D - d0) < kPbChunk ? (D - d0) : kPbChunk);
         if (tid < 2 * kPbTile) {
             const float *row = tid < kPbTile ? cu[tid] : cv[tid - kPbTile];
-            for (int c = 0; c < dn; ++c) nacc = __fmaf_rn(row[c], row[c], nacc);
+#pragma unroll
+            for (int c = 0; c < kPbChunk; c += 4) {
+                const float4 x = *reinterpret_cast<const float4 *>(row + c);
+                nacc = __fmaf_rn(x.x, x.x, nacc);
+                nacc = __fmaf_rn(x.y, x.y, nacc);
+                nacc = __fmaf_rn(x.z, x.z, nacc);
+                nacc = __fmaf_rn(x.w, x.w, nacc);
+            }
         }
-#pragma unroll 8
-        for (int c = 0; c < dn; ++c) {
-            const float t = __fsub_rn(cu[ty][c], cv[tx][c]);
-            acc = __fmaf_rn(t, t, acc);
+#pragma unroll
+        for (int c = 0; c < kPbChunk; c += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(&cu[ty][c]);
+            const float4 b = *reinterpret_cast<const float4 *>(&cv[tx][c]);
+            float t;
+            t = __fsub_rn(a.x, b.x); acc = __fmaf_rn(t, t, acc);
+            t = __fsub_rn(a.y, b.y); acc = __fmaf_rn(t, t, acc);
+            t = __fsub_rn(a.z, b.z); acc = __fmaf_rn(t, t, acc);
+            t = __fsub_rn(a.w, b.w); acc = __fmaf_rn(t, t, acc);
         }
         __syncthreads();
     }
@@ -724,18 +747,20 @@ __device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, int round
             }
         }
         const float2 *row = a.bnd + (int64_t)v * nb;
+        // each lane reads 16 intervals per 512-block batch; a row of at most 512 blocks is read
+        // once and its intervals stay in registers for the candidate pass
+        float2 iv[16];
         float h = __int_as_float(0x7f800000);
         for (int base = 0; base < nb; base += 32 * 16) {
-            float hi[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int u = base + lane + 32 * k;
-                hi[k] = u < nb ? __ldg(&row[u].y) : 0.0f;
+                iv[k] = u < nb ? __ldg(&row[u]) : make_float2(0.0f, 0.0f);
             }
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int u = base + lane + 32 * k;
-                if (u < nb && scomp[u] != cv) h = fminf(h, hi[k]);
+                if (u < nb && scomp[u] != cv) h = fminf(h, iv[k].y);
             }
         }
 #pragma unroll
@@ -744,18 +769,19 @@ __device__ void vertex_min_phase(const GraphArgs &a, const int *scomp, int round
         double bd = __longlong_as_double((long long)kInfBits);
         int ba = INT_MAX, bb = INT_MAX, bu = -1;
         for (int base = 0; base < nb; base += 32 * 16) {
-            float lo[16];
+            if (nb > 32 * 16) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const int u = base + lane + 32 * k;
-                lo[k] = u < nb ? __ldg(&row[u].x) : 0.0f;
+                for (int k = 0; k < 16; ++k) {
+                    const int u = base + lane + 32 * k;
+                    iv[k] = u < nb ? __ldg(&row[u]) : make_float2(0.0f, 0.0f);
+                }
             }
             // lane k keeps the candidate mask of batch slot k
             unsigned mine = 0u;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 const int u = base + lane + 32 * k;
-                const unsigned m = __ballot_sync(0xffffffffu, u < nb && scomp[u] != cv && lo[k] <= h);
+                const unsigned m = __ballot_sync(0xffffffffu, u < nb && scomp[u] != cv && iv[k].x <= h);
                 if (lane == k) mine = m;
             }
 #pragma unroll 1
