@@ -406,7 +406,9 @@ def run_gpu(args):
         "e2e": e2e,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args, w, q.cpu(), k.cpu(), v.cpu(), row_ptr, col_idx, topo)
+        bl = cpu_baseline(args, w, q.cpu(), k.cpu(), v.cpu(), row_ptr, col_idx, topo)
+        bl.pop("_build")
+        line["cpu_baseline"] = bl
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -572,15 +574,19 @@ def run_e2e(args, w, tsa, q, k, v, out, build, row_ptr, col_idx, topo, flops, st
             "call": "tsa_topology_attention_host" if host_call else "torch copies + device calls"}
 
 
-def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo):
-    """The fp64 CPU oracle on the host cores: full schedule build + a sample of attention rows."""
+def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo, reuse_build=None):
+    """The fp64 CPU oracle on the host cores: full schedule build + a sample of attention rows.
+    `reuse_build` = (seconds, row_ptr, col_idx) of a build already timed on this workload: the
+    build is then not run again (it is deterministic) and its measured time is counted."""
     import oracle
 
     threads = os.cpu_count() or 1
     S, D = w.S, w.D
     kh = k.reshape(-1, S, D)
     t0 = time.perf_counter()
-    if args.schedule.startswith("segment:"):
+    if reuse_build is not None:
+        _, rp, ci = reuse_build
+    elif args.schedule.startswith("segment:"):
         rp, ci = oracle.fixed_segment_csr(S, w.block, segment_tokens(args.schedule))
     elif topo:
         tie = "content" if args.schedule == "topology-content" else "index"
@@ -588,7 +594,7 @@ def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo):
     else:
         rp = row_ptr.cpu().numpy()
         ci = col_idx.cpu().numpy()[: rp[-1]]
-    t_build = time.perf_counter() - t0
+    t_build = reuse_build[0] if reuse_build is not None else time.perf_counter() - t0
     rng = np.random.default_rng(0)
     qh, vh = q.reshape(-1, S, D), v.reshape(-1, S, D)
     lens = np.diff(rp).astype(np.float64)
@@ -607,11 +613,14 @@ def cpu_baseline(args, w, q, k, v, row_ptr, col_idx, topo):
     flops_all = visited_flops(int(rp[-1]), w.lanes, D, w.block)
     attn_full_s = t_attn * (flops_all / done_flops)
     step_s = t_build + attn_full_s
+    build_note = "timed on an earlier step, not rerun" if reuse_build is not None else "timed"
     return {"value": round(flops_all / step_s / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
-            "sample": (f"full schedule build ({1e3 * t_build:.1f} ms) + {done_rows} attention rows drawn "
-                       f"uniformly with replacement from the {total_rows} of the workload ({t_attn:.1f} s), "
-                       f"attention extrapolated by visited FLOPs; step estimate {1e3 * step_s:.1f} ms")}
+            "sample": (f"full schedule build ({1e3 * t_build:.1f} ms, {build_note}) + {done_rows} attention "
+                       f"rows drawn uniformly with replacement from the {total_rows} of the workload "
+                       f"({t_attn:.1f} s), attention extrapolated by visited FLOPs; step estimate "
+                       f"{1e3 * step_s:.1f} ms"),
+            "_build": (t_build, rp, ci)}
 
 
 def run_reference(args):
@@ -629,13 +638,19 @@ def run_reference(args):
         rp, ci = oracle.dense_causal_csr(w.nb)
     else:
         rp, ci = build_schedule_host(w, args.schedule)
-    # each step is a bounded sample, so that warm-up + steps stay within a few minutes
-    args.cpu_seconds = 120.0 / max(1, args.warmup + args.steps)
-    times, bl = [], None
+    # each step is a bounded sample, so that warm-up + steps stay within a few minutes: the
+    # attention rows get the per-step budget, and the schedule build (deterministic) is run
+    # again only while it costs at most half of that budget, else its first timing is reused
+    budget = 120.0 / max(1, args.warmup + args.steps)
+    args.cpu_seconds = budget
+    times, bl, reuse = [], None, None
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         bl = cpu_baseline(args, w, q, k, v, torch.as_tensor(rp) if rp is not None else None,
-                          torch.as_tensor(ci) if ci is not None else None, topo)
+                          torch.as_tensor(ci) if ci is not None else None, topo, reuse_build=reuse)
+        build = bl.pop("_build")
+        if reuse is None and build[0] > 0.5 * budget:
+            reuse = build
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
     line = {
