@@ -176,6 +176,64 @@ __global__ void __launch_bounds__(256, 2) centroid_partial_vec8(const uint16_t *
     }
 }
 
+// The same sums for small grids (a few hundred items or fewer, where one thread per item would
+// leave most SMs idle and each thread a long chain of rows): one warp per (lane, block, 8
+// consecutive d).  Lane t adds tokens t, t + 32, ... into the int64 column sums of the path
+// above; the warp then combines them (integer addition is associative, and the exponent range
+// and the out-of-window flag combine by min / max / or), so the sums, and the test of whether
+// they equal the sequential binary64 sum, are those of a single thread walking the block.
+// Columns that fail the test are summed the plain way.
+__global__ void __launch_bounds__(256) centroid_partial_warp(const uint16_t *__restrict__ K, bool bf16, int64_t lanes,
+                                                             int64_t S, int64_t D, int64_t block, int64_t nb,
+                                                             int spread_limit, double *__restrict__ part) {
+    const int lane = threadIdx.x & 31;
+    const int64_t groups = D / 8;
+    const int64_t total = lanes * nb * groups;
+    const int64_t wpb = blockDim.x >> 5;
+    for (int64_t w = blockIdx.x * wpb + (threadIdx.x >> 5); w < total; w += (int64_t)gridDim.x * wpb) {
+        const int64_t g = w % groups;
+        const int64_t lb = w / groups;  // l * nb + b
+        const int64_t l = lb / nb, b = lb % nb;
+        const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
+        const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
+        double *dst = part + lb * D + g * 8;
+        ColumnSum c[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) col_init(c[i]);
+        for (int64_t t = lane; t < n; t += 32) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(src + t * D));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                col_add(c[2 * i], w4[i] & 0xFFFFu, bf16);
+                col_add(c[2 * i + 1], w4[i] >> 16, bf16);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                c[i].acc += __shfl_xor_sync(0xffffffffu, c[i].acc, off);
+                c[i].emin = min(c[i].emin, __shfl_xor_sync(0xffffffffu, c[i].emin, off));
+                c[i].emax = max(c[i].emax, __shfl_xor_sync(0xffffffffu, c[i].emax, off));
+                c[i].bad = __any_sync(0xffffffffu, c[i].bad);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if (lane == i) {
+                if (col_exact(c[i], bf16, n, spread_limit)) {
+                    dst[i] = col_value(c[i], bf16);
+                } else {
+                    double acc = 0.0;
+                    for (int64_t tt = 0; tt < n; ++tt) acc += widen(__ldg(src + tt * D + i), bf16);
+                    dst[i] = acc;
+                }
+            }
+        }
+    }
+}
+
 // Block sums with 16-byte rows streamed: each thread copies its next rows into shared memory
 // with cp.async while it sums earlier ones, so a thread always has loads in flight instead of
 // alternating between loading and summing.  The staging area is [stage][row][thread]
@@ -1290,6 +1348,9 @@ ScheduleWorkspace schedule_workspace_layout(int64_t lanes, int64_t nb, int64_t D
     return w;
 }
 
+// Grids of at most this many (lane, block, 8 d) items sum with a warp per item.
+constexpr int64_t kWarpSumItems = 4096;
+
 // Per-lane block sums of K into part[lanes][nb][D].
 tsa_status launch_block_sums(const ScheduleLaunch &a, double *part) {
     cudaStream_t st = a.stream;
@@ -1301,7 +1362,12 @@ tsa_status launch_block_sums(const ScheduleLaunch &a, double *part) {
     int log2_block = 0;
     while ((int64_t(1) << log2_block) < a.block) ++log2_block;
     const int spread_limit = 45 - log2_block;
-    if (vec && (!a.bf16 || a.block <= 64)) {  // the TwoSum exactness bound holds for <= 64 terms
+    if (vec && (!a.bf16 || a.block <= 64) && items <= kWarpSumItems) {
+        // few items: a warp per item
+        const int64_t nblk = (items + 7) / 8;
+        centroid_partial_warp<<<(unsigned)nblk, 256, 0, st>>>(a.K, a.bf16, a.lanes, a.S, a.D, a.block, a.nb,
+                                                             spread_limit, part);
+    } else if (vec && (!a.bf16 || a.block <= 64)) {  // the TwoSum exactness bound holds for <= 64 terms
         // the small shape only while it fills at most one CTA per SM
         const bool large = items >= (int64_t)152 * 64;
         auto kern = large ? (a.bf16 ? centroid_partial_stream<256, 3, true> : centroid_partial_stream<256, 3, false>)
