@@ -145,6 +145,50 @@ def test_lane_sum_integer_path_and_fallback(spread):
     _assert_same(_gpu_schedule(k, 64, 1, 2, 3), _oracle_schedule(k, 64, 1, 2, 3))
 
 
+def _fuzz_keys(seed):
+    """Seeded keys for the builder fuzz test: one of several distributions that stress the
+    binary32 distance intervals (near-ties, coincident blocks, magnitudes on both sides of the
+    2^+-60 limits where a block's intervals become [0, +inf])."""
+    g = np.random.default_rng(1000 + seed)
+    lanes = int(g.integers(1, 4))
+    block = int(g.choice([1, 4, 16, 64]))
+    nb = int(g.integers(2, 90))
+    D = int(g.choice([1, 2, 5, 16, 64, 128]))
+    kind = seed % 6
+    dtype = torch.bfloat16 if (seed // 6) % 2 == 0 else torch.float16
+    shape = (lanes, nb * block, D)
+    if kind == 0:    # iid Gaussian
+        x = g.normal(size=shape)
+    elif kind == 1:  # few clusters with small noise: many near-equal distances
+        means = g.normal(scale=2.0, size=(4, D))
+        x = means[g.integers(0, 4, size=nb)].repeat(block, axis=0)[None] + g.normal(scale=1e-2, size=shape)
+    elif kind == 2:  # blocks repeated exactly: zero distances and exact ties
+        base = g.normal(size=(lanes, 3 * block, D))
+        x = np.concatenate([base] * (nb // 3 + 1), axis=1)[:, : nb * block]
+    elif kind == 3:  # heavy tails
+        x = g.standard_t(1.5, size=shape)
+    elif kind == 4:  # large magnitudes: around 2^60 in bf16, near the top of the f16 range
+        if dtype == torch.bfloat16:
+            x = g.normal(size=shape) * (2.0 ** g.integers(55, 66))
+        else:
+            x = np.clip(g.normal(size=shape) * 3e4, -6e4, 6e4)
+    else:            # tiny magnitudes around 2^-60 (f16 flushes them to zero or subnormals)
+        x = g.normal(size=shape) * (2.0 ** -g.integers(55, 66))
+    sink, r, topk = int(g.integers(0, 3)), int(g.integers(0, 3)), int(g.integers(0, 6))
+    return torch.as_tensor(x, dtype=torch.float32).to(dtype), block, sink, r, topk, kind
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_builder_fuzz_against_oracle(seed):
+    """Random shapes and distributions: the GPU schedule (built on binary32 distance intervals
+    with exact binary64 keys where they decide) equals the oracle's bit for bit."""
+    k, block, sink, r, topk, kind = _fuzz_keys(seed)
+    assert torch.isfinite(k.float()).all()
+    kd = k.to(DEV)
+    _assert_same(_gpu_schedule(kd, block, sink, r, topk), _oracle_schedule(kd, block, sink, r, topk),
+                 distinct=False)
+
+
 def test_largest_block_count():
     nb = 4096
     gen = torch.Generator().manual_seed(7)

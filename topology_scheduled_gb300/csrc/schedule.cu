@@ -522,12 +522,11 @@ constexpr int kPbFlatBelow = 256;  // nb below which pairwise_bounds_flat runs i
 //   rel     D * 2^-22 (D <= 1024).
 // Error budget; every step below rounds outward, so the interval can only widen:
 //   * |a_d - C_u[d]| <= 2^-24 |C_u[d]| (normal binary32 range, see bounds_copy) and the
-//     binary32 subtraction adds at most 2^-24 |a_d - b_d|, so each difference is off from the
-//     exact C_u[d] - C_v[d] by e_d <= 2^-22 (|a_d| + |b_d|);
-//   * hence the exact sum of (a_d - b_d)^2 (the terms s rounds) is off from the exact
-//     sum of (C_u[d] - C_v[d])^2 by at most sum e_d (2 |a_d - b_d| + e_d)
-//     <= 2^-21 sqrt(N) sqrt(s*) + 2^-44 N, with N = 2 (sum a^2 + sum b^2) >= sum (|a|+|b|)^2
-//     (Cauchy-Schwarz) and s* that exact sum of squares;
+//     binary32 subtraction adds at most 2^-24 |a_d - b_d|, so each computed difference
+//     t_d = fl(a_d - b_d) is off from the exact C_u[d] - C_v[d] by e_d <= 2^-22 (|a_d| + |b_d|);
+//   * hence s* = the exact sum of t_d^2 (the terms s accumulates) is off from the exact sum of
+//     (C_u[d] - C_v[d])^2 by at most sum e_d (2 |t_d| + e_d) <= 2^-21 sqrt(N) sqrt(s*) + 2^-44 N,
+//     with N = 2 (sum a^2 + sum b^2) >= sum (|a_d| + |b_d|)^2 (Cauchy-Schwarz);
 //   * a binary32 recursive sum of D non-negative terms is within a factor 1 -+ D 2^-23 of its
 //     exact value, plus at most D 2^-149 from terms that underflow (inside the 2^-120 slack);
 //   * the binary64 sum rounds each term at most D / 32 + 8 times, so it is within a factor
@@ -559,7 +558,9 @@ __device__ __forceinline__ float2 d2_interval(float s, float na, float nv, float
 constexpr int kPbThreads = kPbTile * kPbTile;
 constexpr int kPbPitch = kPbChunk + 4;  // floats per staged row: 16-byte rows, no bank conflicts
 __global__ void __launch_bounds__(kPbThreads) pairwise_bounds(const float *__restrict__ C, int64_t nb, int64_t D,
-                                                              int tiles, float rel, float2 *__restrict__ B) {
+                                                              int tiles, float rel, float2 *__restrict__ B,
+                                                              unsigned *__restrict__ gbar) {
+    if (blockIdx.x == 0 && threadIdx.x < 4) gbar[threadIdx.x] = 0u;  // the graph kernel's barrier words
     __shared__ __align__(16) float cu[kPbTile][kPbPitch];
     __shared__ __align__(16) float cv[kPbTile][kPbPitch];
     __shared__ float nrm[2 * kPbTile];
@@ -615,7 +616,9 @@ __global__ void __launch_bounds__(kPbThreads) pairwise_bounds(const float *__res
 // thread per pair u < v, 32 pairs per CTA.  The diagonal gets [0, 0] (a block is never an edge
 // of its own component).
 __global__ void __launch_bounds__(32) pairwise_bounds_flat(const float *__restrict__ C, int64_t nb, int64_t D,
-                                                           float rel, float2 *__restrict__ B) {
+                                                           float rel, float2 *__restrict__ B,
+                                                           unsigned *__restrict__ gbar) {
+    if (blockIdx.x == 0 && threadIdx.x < 4) gbar[threadIdx.x] = 0u;  // the graph kernel's barrier words
     const int64_t npairs = nb * (nb - 1) / 2;
     const int64_t p = (int64_t)blockIdx.x * 32 + threadIdx.x;
     if (p < nb) B[p * nb + p] = make_float2(0.0f, 0.0f);
@@ -1434,15 +1437,17 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
             cent, perm, a.nb, a.D, part, cent32);
         graph_cent = part;  // the workspace's block-sum area; centroid_final has read the sums
     }
-    // distance intervals (D <= 1024, so rel = D * 2^-22 is exact and at most 2^-12)
+    // distance intervals (D <= 1024, so rel = D * 2^-22 is exact and at most 2^-12); the kernel
+    // also zeroes the graph kernel's barrier words, which run after it in stream order
+    unsigned *gbar = reinterpret_cast<unsigned *>(w + ws.gbar);
     const float rel = ldexpf((float)a.D, -22);
     if (nb < kPbFlatBelow) {
         const int64_t npairs = a.nb * (a.nb - 1) / 2;
         const int64_t n = npairs > a.nb ? npairs : a.nb;
-        pairwise_bounds_flat<<<(unsigned)((n + 31) / 32), 32, 0, st>>>(cent32, a.nb, a.D, rel, bnd);
+        pairwise_bounds_flat<<<(unsigned)((n + 31) / 32), 32, 0, st>>>(cent32, a.nb, a.D, rel, bnd, gbar);
     } else {
         const int t = (nb + kPbTile - 1) / kPbTile;
-        pairwise_bounds<<<(unsigned)(t * (t + 1) / 2), kPbThreads, 0, st>>>(cent32, a.nb, a.D, t, rel, bnd);
+        pairwise_bounds<<<(unsigned)(t * (t + 1) / 2), kPbThreads, 0, st>>>(cent32, a.nb, a.D, t, rel, bnd, gbar);
     }
     // MST, elder rule and CSR in one cooperative launch
     int rounds = 0;
@@ -1470,8 +1475,6 @@ tsa_status launch_schedule_from_sums(const ScheduleLaunch &a, const double *sums
     if (ggrid > sms * per_sm) ggrid = sms * per_sm;
     if (ggrid > sms) ggrid = sms;
     if (ggrid < 1) ggrid = 1;
-    unsigned *gbar = reinterpret_cast<unsigned *>(w + ws.gbar);
-    if (cudaMemsetAsync(gbar, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return TSA_ERR_CUDA;
     GraphArgs g;
     g.bnd = bnd;
     g.cent = graph_cent;
