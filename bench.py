@@ -48,7 +48,9 @@ import torch  # noqa: E402
 from topology_scheduled_gb300.workloads import WORKLOADS, make_qkv, random_density_csr  # noqa: E402
 
 DEFAULT_WORKLOAD = "b2h32s32768"
-ATTN_SOURCE = os.path.join(ROOT, "topology_scheduled_gb300", "csrc", "attention.cu")
+# the attention kernel's sources: a traffic record applies only to the build it was taken on
+ATTN_SOURCES = [os.path.join(ROOT, "topology_scheduled_gb300", "csrc", f)
+                for f in ("attention.cu", "tsa_device.cuh", "tsa_internal.h")]
 
 
 def parse():
@@ -122,6 +124,15 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def attention_sources_sha1() -> str:
+    """sha1 over the attention kernel's source files, concatenated in a fixed order."""
+    h = hashlib.sha1()
+    for path in ATTN_SOURCES:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def attention_traffic_per_launch(workload: str, schedule: str):
     """DRAM bytes per attention launch from the committed ncu summary, if it matches the source."""
     path = os.path.join(ROOT, "profiles", "attention_traffic.json")
@@ -129,10 +140,9 @@ def attention_traffic_per_launch(workload: str, schedule: str):
         return None
     with open(path) as f:
         rec = json.load(f)
-    with open(ATTN_SOURCE, "rb") as f:
-        digest = hashlib.sha1(f.read()).hexdigest()
+    digest = attention_sources_sha1()
     entry = rec.get(f"{workload}/{schedule}")
-    if not entry or entry.get("attention_cu_sha1") != digest:
+    if not entry or entry.get("sources_sha1") != digest:
         return None
     return entry.get("dram_bytes_per_launch")
 

@@ -692,7 +692,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         tma_store_2d(&tmO, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
                 }
                 tma_store_commit();
-                tma_store_wait_all();
+                tma_store_wait_read();
             }
         }
     }

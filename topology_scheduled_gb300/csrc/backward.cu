@@ -702,7 +702,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
                         tma_store_2d(&tmdQ, c * 64, row0 + (qa + 1) * kBlock, sQ + c * 16384 + 8192);
                 }
                 tma_store_commit();
-                tma_store_wait_all();
+                tma_store_wait_read();
             }
             if ((half ? part_b : part_a) && qa * kBlock + tid < S)
                 copy_staged_row<D>(smem + (sQ - base), tid, dQ + ((size_t)row0 + qa * kBlock + tid) * D);
@@ -1024,7 +1024,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                     }
                 }
                 tma_store_commit();
-                tma_store_wait_all();
+                tma_store_wait_read();
             }
             if ((half ? part_b : part_a) && key_block * kBlock + k_in < S) {
                 const size_t grow_k = ((size_t)row0 + key_block * kBlock + k_in) * D;

@@ -134,8 +134,11 @@ __device__ __forceinline__ void tma_store_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_store_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+// Waits until every committed bulk store has finished reading its shared-memory source (the
+// global writes complete on their own before the grid does).  Enough before a CTA exits, or
+// before the staging tile is written again.
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
