@@ -304,12 +304,6 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     using L = AttnSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
 
-    // A launch that already gave up elsewhere: leave before taking any resource (one thread
-    // reads the flag so that the whole CTA takes the same branch).
-    if (__syncthreads_or(threadIdx.x == 0 &&
-                         *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch))
-        return;
-
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     if (base - raw_base + L::kOffMeta + L::kMetaBytes > (uint32_t)kAttnSmemBytes<D>()) {
@@ -341,6 +335,16 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     const bool has_b = qa + 1 < nb;
     const int row0 = lane_id * S;                    // first row of this lane in [L*S, D]
 
+    // The first global reads are issued together and waited for at the barrier below: whether
+    // the launch already gave up elsewhere (one thread reads the flag, so the whole CTA takes
+    // the same branch), and the producer's CSR rows.
+    const bool gave_up = tid == 0 && *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch;
+    EntryWalk<kGran> ruk, ruv;  // the producer's walks of the row union, one per stream
+    if (tid == kProducerWarp * 32) {
+        ruk.init(row_ptr, col_idx, qa, has_b, nb, S);
+        ruv.init(row_ptr, col_idx, qa, has_b, nb, S);
+    }
+
     if (tid == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < kKStages; ++s) {
@@ -366,9 +370,13 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    const bool leave = __syncthreads_or(gave_up);
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kOffMeta + kTmemSlot);
+    if (leave) {  // nothing was issued yet: give the columns back and go
+        if (warp == kMmaWarp) tmem_dealloc(tmem, L::kTmemCols);
+        return;
+    }
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ producer (TMA)
@@ -381,9 +389,6 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmO);
-            EntryWalk<kGran> ruk, ruv;  // each stream walks the row union on its own
-            ruk.init(row_ptr, col_idx, qa, has_b, nb, S);
-            ruv.init(row_ptr, col_idx, qa, has_b, nb, S);
             mbar_arrive_expect_tx(bar_q, L::kQBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c)
