@@ -189,6 +189,21 @@ def test_builder_fuzz_against_oracle(seed):
                  distinct=False)
 
 
+@pytest.mark.parametrize("D,dtype", [(1000, torch.bfloat16), (1024, torch.float16), (1024, torch.bfloat16)])
+def test_widest_head_dim(D, dtype):
+    """The builder's widest head dimension (1024; the distance intervals' error budget is sized
+    for it) and a width that is not a multiple of 32: bit-exact CSR and salience, with keys
+    drawn around 8 cluster means so that many distances nearly tie."""
+    g = torch.Generator().manual_seed(D)
+    nb, block, lanes = 60, 4, 2
+    means = torch.randn((8, D), generator=g)
+    which = torch.randint(0, 8, (nb,), generator=g)
+    x = means[which].repeat_interleave(block, dim=0)[None].repeat(lanes, 1, 1)
+    x = x + 0.01 * torch.randn((lanes, nb * block, D), generator=g)
+    kd = x.to(dtype).to(DEV)
+    _assert_same(_gpu_schedule(kd, block, 1, 2, 4), _oracle_schedule(kd, block, 1, 2, 4), distinct=False)
+
+
 def test_largest_block_count():
     nb = 4096
     gen = torch.Generator().manual_seed(7)

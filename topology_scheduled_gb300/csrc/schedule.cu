@@ -250,6 +250,15 @@ __global__ void __launch_bounds__(256) centroid_partial_warp(const uint16_t *__r
 // hi + lo is the exact column sum.  That sum has at most e_max - e_min + 14 <= 42 significant
 // bits, so the sequential binary64 sum is exact too and both equal (double)hi + (double)lo.
 // Other columns take the sequential binary64 loop (column_sum_exact_slow).
+//
+// f16 keys in blocks of at most 64 tokens take the same pair (the int64 path costs ~15 integer
+// operations per element and left the pass ALU-bound).  With biased exponents E (subnormals
+// counted as 1) every element and every error is a multiple of 2^(E_min - 25), each element is
+// below 2^(E_max - 14) and hi below 2^(E_max - 8), so each error is below 2^(E_max - 33) and
+// lo's partial sums below 2^(E_max - 27): E_max - E_min - 2 significant bits, exact in fp32
+// for E_max - E_min <= 26 (25 is required, and E_max <= 30: no inf/nan).  The column sum then
+// has at most E_max - E_min + 17 <= 42 significant bits, so as above the sequential binary64
+// sum is exact and equals (double)hi + (double)lo.
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -266,10 +275,13 @@ struct StreamShape {
     static constexpr int kSmem = kStages * 8 * kThreads * 16;
 };
 
-template <int kThreads, int kStages, bool kBF16>
+// kTwoSum: the hi + lo pair (bf16, or f16 in blocks of at most 64 tokens); otherwise the
+// int64 column sums (f16 in longer blocks).
+template <int kThreads, int kStages, bool kBF16, bool kTwoSum>
 __global__ void __launch_bounds__(kThreads, kThreads == 256 ? 2 : 1)
 centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S, int64_t D, int64_t block,
                         int64_t nb, int spread_limit, double *__restrict__ part) {
+    static_assert(kTwoSum || !kBF16, "bf16 keys take the pair");
     extern __shared__ __align__(16) uint4 stage[];
     const uint32_t stage0 = smem_u32(stage) + threadIdx.x * 16u;
     const int64_t groups = D / 8;
@@ -282,11 +294,11 @@ centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S
         const int64_t n = (b + 1) * block <= S ? block : S - b * block;  // tokens in the block
         const uint16_t *src = K + ((l * S + b * block) * D + g * 8);
         double *dst = part + lb * D + g * 8;
-        // bf16 state: hi + lo pairs and packed |bits| max/min; f16 state: int64 column sums
+        // pair state: hi + lo pairs and packed |bits| max/min; otherwise int64 column sums
         uint64_t hi[4], lo[4];
         uint32_t mx[4], mn[4];
-        ColumnSum cs[kBF16 ? 1 : 8];
-        if constexpr (kBF16) {
+        ColumnSum cs[kTwoSum ? 1 : 8];
+        if constexpr (kTwoSum) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 hi[i] = f2_pack(0.f, 0.f);
@@ -299,9 +311,15 @@ centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S
             for (int i = 0; i < 8; ++i) col_init(cs[i]);
         }
         auto add_word = [&](int i, uint32_t x) {
-            if constexpr (kBF16) {
+            if constexpr (kTwoSum) {
                 // hi + lo += x exactly (TwoSum), two columns per packed operation
-                const uint64_t v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+                uint64_t v;
+                if constexpr (kBF16) {
+                    v = f2_pack(__uint_as_float(x << 16), __uint_as_float(x & 0xFFFF0000u));
+                } else {
+                    const float2 xf = __half22float2(*reinterpret_cast<const __half2 *>(&x));
+                    v = f2_pack(xf.x, xf.y);  // low half first, as for bf16
+                }
                 const uint64_t s = f2_add(hi[i], v);
                 const uint64_t bv = f2_sub(s, hi[i]);
                 const uint64_t err = f2_add(f2_sub(hi[i], f2_sub(s, bv)), f2_sub(v, bv));
@@ -345,7 +363,10 @@ centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S
         }
         cp_async_wait<0>();
         for (int64_t t = full; t < n; ++t) add_row(__ldg(reinterpret_cast<const uint4 *>(src + t * D)));
-        if constexpr (kBF16) {
+        if constexpr (kTwoSum) {
+            constexpr int kMantBits = kBF16 ? 7 : 10;     // explicit mantissa bits
+            constexpr int kMaxExp = kBF16 ? 240 : 30;     // no fp32 overflow / no inf, nan
+            constexpr int kMaxSpread = kBF16 ? 28 : 25;   // lo stays exact (see above)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float h0, h1, l0, l1;
@@ -355,12 +376,12 @@ centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
                     const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
-                    const int emax = (int)(amax >> 7);
-                    const int emin = max(1, (int)(amin >> 7));
+                    const int emax = (int)(amax >> kMantBits);
+                    const int emin = max(1, (int)(amin >> kMantBits));
                     const bool all_zero = amin == 0xFFFFu;
-                    const bool exact = all_zero || (emax <= 240 && emax - emin <= 28);
+                    const bool exact = all_zero || (emax <= kMaxExp && emax - emin <= kMaxSpread);
                     dst[2 * i + h] = exact ? (double)(h ? h1 : h0) + (double)(h ? l1 : l0)
-                                           : column_sum_exact_slow(src + 2 * i + h, D, n, true, spread_limit);
+                                           : column_sum_exact_slow(src + 2 * i + h, D, n, kBF16, spread_limit);
                 }
             }
         } else {
@@ -1373,8 +1394,14 @@ tsa_status launch_block_sums(const ScheduleLaunch &a, double *part) {
     } else if (vec && (!a.bf16 || a.block <= 64)) {  // the TwoSum exactness bound holds for <= 64 terms
         // the small shape only while it fills at most one CTA per SM
         const bool large = items >= (int64_t)152 * 64;
-        auto kern = large ? (a.bf16 ? centroid_partial_stream<256, 3, true> : centroid_partial_stream<256, 3, false>)
-                          : (a.bf16 ? centroid_partial_stream<64, 8, true> : centroid_partial_stream<64, 8, false>);
+        // the pair for bf16, and for f16 in blocks of at most 64 tokens (its exactness bound)
+        const bool pair = a.bf16 || a.block <= 64;
+        auto kern = large ? (a.bf16 ? centroid_partial_stream<256, 3, true, true>
+                                    : pair ? centroid_partial_stream<256, 3, false, true>
+                                           : centroid_partial_stream<256, 3, false, false>)
+                          : (a.bf16 ? centroid_partial_stream<64, 8, true, true>
+                                    : pair ? centroid_partial_stream<64, 8, false, true>
+                                           : centroid_partial_stream<64, 8, false, false>);
         const int nthr = large ? 256 : 64;
         const int smem = large ? StreamShape<256, 3>::kSmem : StreamShape<64, 8>::kSmem;
         const int64_t nblk = (items + nthr - 1) / nthr;
