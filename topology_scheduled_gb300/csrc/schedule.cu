@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(32) pairwise_bounds_flat(const float *__restri
 }
 
 // ---------------------------------------------------------------- MST, elder rule, CSR
-// One cooperative launch runs everything after the distance matrix.  Its CTAs are all
+// One cooperative launch runs everything after the distance intervals.  Its CTAs are all
 // resident (cudaLaunchCooperativeKernel), so they can meet at grid-wide barriers; the barrier
 // is bounded in time like every other wait here.
 //   Boruvka rounds: all warps find each vertex's lightest edge to another component (strict
