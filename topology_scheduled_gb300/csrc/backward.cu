@@ -440,9 +440,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
               float scale, float scale_log2, uint16_t *__restrict__ dQ, DeviceFlags flags) {
     using L = DqSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    if (__syncthreads_or(threadIdx.x == 0 &&
-                         *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch))
-        return;
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     if (base - raw_base + L::kOffMeta + kMetaBytes > (uint32_t)L::kBytes) {
@@ -470,6 +467,20 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const bool has_b = qa + 1 < nb;
     const int row0 = lane_id * S;
 
+    // The first global reads are issued together and waited for at the barrier below: whether
+    // the launch already gave up elsewhere (one thread, so the whole CTA takes the same branch),
+    // and the producer's two CSR rows.
+    const bool gave_up = tid == 0 && *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch;
+    ListUnion lu;
+    if (tid == kProducerWarp * 32) {
+        lu.a = col_idx + row_ptr[qa];
+        lu.ia = 0;
+        lu.ia_end = vlen[qa];
+        lu.b = has_b ? col_idx + row_ptr[qa + 1] : col_idx;
+        lu.ib = 0;
+        lu.ib_end = has_b ? vlen[qa + 1] : 0;
+    }
+
     if (tid == 0) {
         mbar_init(bar_tile, 1);
         for (int s = 0; s < kStream; ++s) {
@@ -493,9 +504,13 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    const bool leave = __syncthreads_or(gave_up);
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kOffMeta + kTmemSlot);
+    if (leave) {  // nothing was issued yet: give the columns back and go
+        if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
 
     if (warp == kProducerWarp) {
         if ((tid & 31) == 0) {
@@ -504,13 +519,6 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             tma_prefetch_desc(&tmdQ);
-            ListUnion lu;
-            lu.a = col_idx + row_ptr[qa];
-            lu.ia = 0;
-            lu.ia_end = vlen[qa];
-            lu.b = has_b ? col_idx + row_ptr[qa + 1] : col_idx;
-            lu.ib = 0;
-            lu.ib_end = has_b ? vlen[qa + 1] : 0;
             mbar_arrive_expect_tx(bar_tile, 2 * L::kTileBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
@@ -753,9 +761,6 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                uint16_t *__restrict__ dK, uint16_t *__restrict__ dV, DeviceFlags flags) {
     using L = DkvSmem<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    if (__syncthreads_or(threadIdx.x == 0 &&
-                         *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch))
-        return;
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     if (base - raw_base + L::kOffMeta + kMetaBytes > (uint32_t)L::kBytes) {
@@ -784,6 +789,19 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
     const bool has_b = kb >= 0;
     const int row0 = lane_id * S;
 
+    // As in the dQ kernel: the abort flag and the producer's two transposed columns are read
+    // before the first barrier.
+    const bool gave_up = tid == 0 && *reinterpret_cast<volatile unsigned *>(flags.abort_epoch) == flags.epoch;
+    ListUnion lu;
+    if (tid == kProducerWarp * 32) {
+        lu.a = row_idx + col_ptr[ka];
+        lu.ia = 0;
+        lu.ia_end = col_ptr[ka + 1] - col_ptr[ka];
+        lu.b = has_b ? row_idx + col_ptr[kb] : row_idx;
+        lu.ib = 0;
+        lu.ib_end = has_b ? col_ptr[kb + 1] - col_ptr[kb] : 0;
+    }
+
     if (tid == 0) {
         mbar_init(bar_tile, 1);
         for (int s = 0; s < kStream; ++s) {
@@ -805,9 +823,13 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    const bool leave = __syncthreads_or(gave_up);
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + L::kOffMeta + kTmemSlot);
+    if (leave) {  // nothing was issued yet: give the columns back and go
+        if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+        return;
+    }
     constexpr uint32_t kDVCol = kAccCol, kDKCol = kAccCol + D;
 
     if (warp == kProducerWarp) {
@@ -818,13 +840,6 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
             tma_prefetch_desc(&tmdO);
             tma_prefetch_desc(&tmdK);
             tma_prefetch_desc(&tmdV);
-            ListUnion lu;
-            lu.a = row_idx + col_ptr[ka];
-            lu.ia = 0;
-            lu.ia_end = col_ptr[ka + 1] - col_ptr[ka];
-            lu.b = has_b ? row_idx + col_ptr[kb] : row_idx;
-            lu.ib = 0;
-            lu.ib_end = has_b ? col_ptr[kb + 1] - col_ptr[kb] : 0;
             mbar_arrive_expect_tx(bar_tile, 2 * L::kTileBytes);
 #pragma unroll
             for (int c = 0; c < L::kChunks; ++c) {
