@@ -271,39 +271,52 @@ __device__ __forceinline__ float to_f32(uint32_t h16) {
     else return __half2float(__ushort_as_half((unsigned short)h16));
 }
 
-// D/8 threads per row, 16-byte loads, fp32 products summed in the thread then across the group.
-// Rows are laid out per lane over Sp = nb * 64 tokens; the tokens past S (a partial last block)
-// get Delta 0 and log-sum-exp -inf, and the given log-sum-exp is copied into the same layout.
-template <bool kBF16>
-__global__ void bwd_delta(const uint16_t *__restrict__ O, const uint16_t *__restrict__ dO,
-                          const float *__restrict__ lse, long long lanes, int S, int Sp, int D,
-                          float *__restrict__ delta, float *__restrict__ lse_pad) {
-    const int g = D >> 3;  // 8 or 16 lanes per row, so a row never straddles a warp
-    const long long total = lanes * Sp * g;
-    const long long stride = (long long)gridDim.x * blockDim.x;
-    for (long long base = (long long)blockIdx.x * blockDim.x; base < total; base += stride) {
-        const long long x = base + threadIdx.x;
-        float acc = 0.f;
-        const long long pr = x / g;          // padded row
-        const long long l = pr / Sp;
-        const int t = (int)(pr % Sp);        // token within the lane
-        const bool real = x < total && t < S;
-        const long long r = l * S + t;       // row of O, dO and lse
-        if (real) {
-            const int c = (int)(x % g);
-            const uint4 a = __ldg(reinterpret_cast<const uint4 *>(O + r * D + c * 8));
-            const uint4 b = __ldg(reinterpret_cast<const uint4 *>(dO + r * D + c * 8));
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+// Delta per row in fp32.  kG = D / 8 threads per row (8 or 16, so a row never straddles a warp),
+// each reading 16 bytes of O and of dO; products summed in the thread, then across the group.
+// Grid: y over lanes, x over a lane's (row, 16-byte chunk) items -- at most 8192 * 64 * 16, so
+// 32-bit indices and shifts -- with four items per thread whose loads are all issued before
+// their arithmetic.  Rows are laid out per lane over Sp = nb * 64 tokens; the tokens past S (a
+// partial last block) get Delta 0 and log-sum-exp -inf, and the given log-sum-exp is copied
+// into the same layout.
+constexpr int kDeltaItems = 4;
+template <bool kBF16, int kG>
+__global__ void __launch_bounds__(256) bwd_delta(const uint16_t *__restrict__ O, const uint16_t *__restrict__ dO,
+                                                 const float *__restrict__ lse, int S, int Sp,
+                                                 float *__restrict__ delta, float *__restrict__ lse_pad) {
+    constexpr int D = kG * 8;
+    const long long lane = blockIdx.y;
+    const int per_lane = Sp * kG;
+    const int first = (int)blockIdx.x * (int)blockDim.x * kDeltaItems + (int)threadIdx.x;
+    uint4 a[kDeltaItems], b[kDeltaItems];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                acc = fmaf(to_f32<kBF16>(av[t] & 0xFFFFu), to_f32<kBF16>(bv[t] & 0xFFFFu), acc);
-                acc = fmaf(to_f32<kBF16>(av[t] >> 16), to_f32<kBF16>(bv[t] >> 16), acc);
-            }
+    for (int k = 0; k < kDeltaItems; ++k) {
+        const int x = first + k * (int)blockDim.x;
+        const int t = x / kG;  // token within the lane
+        if (x < per_lane && t < S) {
+            const size_t off = (size_t)(lane * S + t) * D + (size_t)(x % kG) * 8;
+            a[k] = __ldg(reinterpret_cast<const uint4 *>(O + off));
+            b[k] = __ldg(reinterpret_cast<const uint4 *>(dO + off));
+        } else {
+            a[k] = b[k] = make_uint4(0u, 0u, 0u, 0u);
         }
-        for (int off = g >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (x < total && (x % g) == 0) {
+    }
+#pragma unroll
+    for (int k = 0; k < kDeltaItems; ++k) {
+        const int x = first + k * (int)blockDim.x;
+        const int t = x / kG;
+        const uint32_t av[4] = {a[k].x, a[k].y, a[k].z, a[k].w}, bv[4] = {b[k].x, b[k].y, b[k].z, b[k].w};
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            acc = fmaf(to_f32<kBF16>(av[q] & 0xFFFFu), to_f32<kBF16>(bv[q] & 0xFFFFu), acc);
+            acc = fmaf(to_f32<kBF16>(av[q] >> 16), to_f32<kBF16>(bv[q] >> 16), acc);
+        }
+#pragma unroll
+        for (int off = kG >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (x < per_lane && x % kG == 0) {
+            const long long pr = lane * Sp + t;  // padded row
             delta[pr] = acc;
-            lse_pad[pr] = real ? __ldg(lse + r) : -INFINITY;
+            lse_pad[pr] = t < S ? __ldg(lse + lane * S + t) : -INFINITY;
         }
     }
 }
@@ -1142,13 +1155,17 @@ tsa_status launch_attention_backward(const BwdLaunch &a_in) {
     }
     {
         const int Sp = a.nb * kBlock;
-        const long long items = (long long)a.lanes * Sp * (a.D / 8);
-        const long long blocks = (items + 255) / 256;
-        const unsigned g = (unsigned)(blocks < 152 * 32 ? blocks : 152 * 32);
-        if (a.bf16)
-            bwd_delta<true><<<g, 256, 0, st>>>(a.O, a.dO, a.lse, a.lanes, a.S, Sp, a.D, a.delta, a.lse_pad);
-        else
-            bwd_delta<false><<<g, 256, 0, st>>>(a.O, a.dO, a.lse, a.lanes, a.S, Sp, a.D, a.delta, a.lse_pad);
+        const int per_lane = Sp * (a.D / 8);
+        const dim3 grid((unsigned)((per_lane + 256 * kDeltaItems - 1) / (256 * kDeltaItems)), (unsigned)a.lanes);
+        if (a.D == 128) {
+            if (a.bf16) bwd_delta<true, 16><<<grid, 256, 0, st>>>(a.O, a.dO, a.lse, a.S, Sp, a.delta, a.lse_pad);
+            else bwd_delta<false, 16><<<grid, 256, 0, st>>>(a.O, a.dO, a.lse, a.S, Sp, a.delta, a.lse_pad);
+        } else if (a.D == 64) {
+            if (a.bf16) bwd_delta<true, 8><<<grid, 256, 0, st>>>(a.O, a.dO, a.lse, a.S, Sp, a.delta, a.lse_pad);
+            else bwd_delta<false, 8><<<grid, 256, 0, st>>>(a.O, a.dO, a.lse, a.S, Sp, a.delta, a.lse_pad);
+        } else {
+            return TSA_ERR_UNSUPPORTED;
+        }
     }
     if (cudaGetLastError() != cudaSuccess) return TSA_ERR_CUDA;
     if (a.D == 64) return a.bf16 ? launch_grad_kernels<64, true>(a) : launch_grad_kernels<64, false>(a);
