@@ -377,6 +377,18 @@ tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const voi
  */
 tsa_status tsa_last_device_status(tsa_stream_t stream);
 
+/*
+ * Test hook for the failure path (no counterpart on the pages).  With `on` = 1, every later
+ * scheduled-attention launch of this process has its first CTA withhold the scores of its
+ * first key block, so that CTA's softmax wait runs out after its bound (1 s): the launch
+ * gives up cleanly -- no trap, no hang; every CTA drains what it issued and frees its
+ * tensor memory -- and tsa_last_device_status() then reports TSA_ERR_TIMEOUT.  The output of
+ * such a launch is unspecified.  `on` = 0 restores normal launches (the default); the CUDA
+ * context stays usable throughout.  Process-wide, not thread-safe against concurrent
+ * launches, and meant for tests only.  TSA_ERR_INVALID_ARGUMENT for other values.
+ */
+tsa_status tsa_debug_set_wait_injection(int on);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ def _declared():
 def test_every_declared_symbol_is_exported_and_bound():
     L = tsa.lib()
     names = _declared()
-    assert len(names) == 18
+    assert len(names) == 19
     for n in names:
         assert hasattr(L, n), n
         assert n in SIGNATURES, n

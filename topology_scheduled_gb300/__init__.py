@@ -22,4 +22,5 @@ from .binding import (STATUS_NAMES, TIE_RULES, TSA_BF16, TSA_F16, TsaError, lib,
                       tsa_last_device_status, tsa_schedule_max_nnz, tsa_scheduled_attention,
                       tsa_scheduled_attention_fwd, tsa_scheduled_attention_backward,
                       tsa_attention_backward_workspace_bytes, tsa_segment_csr, tsa_block_sums,
-                      tsa_build_schedule_from_sums, tsa_topology_attention_host)
+                      tsa_build_schedule_from_sums, tsa_topology_attention_host,
+                      tsa_debug_set_wait_injection)

@@ -52,6 +52,7 @@ SIGNATURES = {
     "tsa_scheduled_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
                                                _I64, _I64, _I64, ctypes.c_float, _P]),
     "tsa_last_device_status": (ctypes.c_int, [_P]),
+    "tsa_debug_set_wait_injection": (ctypes.c_int, [ctypes.c_int]),
     "tsa_scheduled_attention_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, ctypes.c_int, _I64, _I64,
                                                    _I64, _I64, _I64, ctypes.c_float, _P]),
     "tsa_attention_backward_workspace_bytes": (_SZ, [_I64, _I64, _I64, _I64]),
@@ -362,6 +363,13 @@ def tsa_scheduled_attention_backward(Q, K, V, O, dO, lse, row_ptr, col_idx, scal
 def tsa_last_device_status(stream=None) -> int:
     """Synchronizes the stream; returns and clears the device status word (0 = TSA_OK)."""
     return int(lib().tsa_last_device_status(_stream(stream)))
+
+
+def tsa_debug_set_wait_injection(on: bool) -> None:
+    """Test hook for the failure path: while on, each scheduled-attention launch has its first
+    CTA withhold its first scores, so a bounded wait runs out and the device status reports
+    TSA_ERR_TIMEOUT (see include/tsa.h)."""
+    _check(lib().tsa_debug_set_wait_injection(1 if on else 0), "tsa_debug_set_wait_injection")
 
 
 def tsa_topology_attention_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, block: int = 64,

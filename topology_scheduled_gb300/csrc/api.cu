@@ -40,6 +40,9 @@ tsa_status current_device(int *dev) {
 }
 
 // Device addresses of the status words (looked up once per device) and a fresh epoch.
+// Process-wide test hook for the failure path (tsa_debug_set_wait_injection).
+std::atomic<unsigned> g_wait_injection{0u};
+
 tsa_status device_flags(int dev, DeviceFlags *f) {
     {
         std::lock_guard<std::mutex> lock(g_mutex);
@@ -61,6 +64,7 @@ tsa_status device_flags(int dev, DeviceFlags *f) {
         e = ++g_epoch;
     } while (e == 0u || e == ~0u);
     f->epoch = e;
+    f->inject = g_wait_injection.load();
     return TSA_OK;
 }
 
@@ -567,6 +571,12 @@ tsa_status tsa_last_device_status(tsa_stream_t stream) {
     if (bits & kDevTimeout) return TSA_ERR_TIMEOUT;
     if (bits & kDevBadSchedule) return TSA_ERR_BAD_SCHEDULE;
     if (bits) return TSA_ERR_DEVICE;
+    return TSA_OK;
+}
+
+tsa_status tsa_debug_set_wait_injection(int on) {
+    if (on != 0 && on != 1) return TSA_ERR_INVALID_ARGUMENT;
+    g_wait_injection.store((unsigned)on);
     return TSA_OK;
 }
 

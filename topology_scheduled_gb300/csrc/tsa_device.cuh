@@ -28,6 +28,8 @@ struct DeviceFlags {
     unsigned *status;       // sticky error bits
     unsigned *abort_epoch;  // epoch of the launch that gave up; later CTAs of it exit early
     unsigned epoch;         // this launch's epoch
+    unsigned inject;        // test hook (tsa_debug_set_wait_injection): 1 = the attention's first
+                            // CTA withholds its first score tile, so a bounded wait runs out
 };
 
 __device__ __forceinline__ void raise_status(const DeviceFlags &f, unsigned bit) {
