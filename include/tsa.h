@@ -314,7 +314,12 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
  * device memory for its own pool, or a latency-bound loop in which cudaMalloc's implicit
  * device-wide synchronization is not acceptable.  This entry point takes no workspace; it
  * uses a fixed scratch array of TSA_NOALLOC_SCRATCH_BYTES inside the library instead and
- * calls no allocating routine.  The paper has no counterpart: this is a packaging choice of
+ * calls no cudaMalloc, cudaFree or other allocating routine.  One caveat for the first call
+ * on a device: it looks up the array's device address, and with lazy module loading (the
+ * CUDA runtime's default) that lookup may load this library's module on the device and
+ * reserve the array's memory right then, which can synchronize the device.  Make that first
+ * call outside any latency-critical region and before any stream capture; later calls do
+ * neither.  The paper has no counterpart: this is a packaging choice of
  * this library, not part of the method.
  *
  * Arguments, results and limits are those of tsa_build_schedule without `workspace` and
@@ -324,7 +329,7 @@ tsa_status tsa_scheduled_attention_backward(const void *Q, const void *K, const 
  * 64 lanes of [8192, 64] need about 4.2 MiB and fit).
  *
  * The first call on each device looks up the scratch array's device address (with that
- * device current) and caches it; make that first call before any stream capture.  All calls
+ * device current) and caches it (see above).  All calls
  * on a device share the one array: calls that can overlap on the GPU (on different streams
  * without ordering between them) race on it and must be serialized by the caller.  Nothing
  * in the array needs to start at zero; a call never reads what an earlier call left there.
@@ -342,9 +347,11 @@ tsa_status tsa_build_schedule_noalloc(const void *K, tsa_dtype dtype, int64_t la
  * sixteenth of the lanes): the K chunks are copied first and each one's block sums run as soon
  * as it lands, then the schedule; the Q and V chunks follow, each chunk's attention starts
  * when its Q and V have landed, and its O is copied back on a third stream while the next
- * chunk runs.  The copies use two streams of the library's own, created and released inside
- * the call; the work runs on `stream`, and `stream` continues only after every copy has been
- * made (the call is asynchronous like the others: synchronize `stream` before reading hO).
+ * chunk runs.  The copies use two streams and a set of events of the library's own, created by
+ * the first call on each device and kept until the process exits (calls on one device from
+ * several host threads take turns enqueueing); the work runs on `stream`, and `stream`
+ * continues only after every copy has been made (the call is asynchronous like the others:
+ * synchronize `stream` before reading hO).
  *
  *   hQ, hK, hV   in, [B*H, S, D] of `dtype` in host memory (page-locked for the copies to run
  *                asynchronously and overlap; pageable memory works, slower)

@@ -173,6 +173,8 @@ size_t tsa_build_schedule_workspace_bytes(int64_t lanes, int64_t S, int64_t D, i
     if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0) return 0;
     const int64_t nb = (S + block - 1) / block;
     if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return 0;
+    // the block sums alone are 8 * lanes * nb * D bytes: refuse sizes whose total would wrap
+    if (lanes > INT64_MAX / S / D || lanes > INT64_MAX / 16 / nb / D) return 0;
     return schedule_workspace_layout(lanes, nb, D).total;
 }
 
@@ -200,7 +202,7 @@ tsa_status tsa_build_schedule_ex(const void *K, tsa_dtype dtype, int64_t lanes, 
         return TSA_ERR_INVALID_ARGUMENT;
     const int64_t nb = (S + block - 1) / block;  // a partial last block counts
     if (nb > kMaxScheduleBlocks || D > kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
-    if (lanes > INT64_MAX / S / D) return TSA_ERR_INVALID_ARGUMENT;
+    if (lanes > INT64_MAX / S / D || lanes > INT64_MAX / 16 / nb / D) return TSA_ERR_INVALID_ARGUMENT;
     const int64_t need = max_nnz_bound(nb, sink, local_radius, topk);
     if (col_cap < need) return TSA_ERR_CAPACITY;
     const ScheduleWorkspace ws = schedule_workspace_layout(lanes, nb, D);
@@ -413,6 +415,8 @@ tsa_status tsa_scheduled_attention_fwd(const void *Q, const void *K, const void 
 
 namespace tsa {
 namespace {
+
+constexpr int kHostStepDevices = 64;
 // The attention launch once the arguments have been checked.
 tsa_status launch_attention_checked(const void *Q, const void *K, const void *V, const int32_t *row_ptr,
                                     const int32_t *col_idx, void *O, float *lse, bool bf16, int64_t lanes,
@@ -443,6 +447,40 @@ tsa_status launch_attention_checked(const void *Q, const void *K, const void *V,
     TSA_TRY(device_flags(dev, &a.flags));
     return launch_scheduled_attention(a);
 }
+// Copy streams and events of tsa_topology_attention_host, created on the first call on each
+// device and kept for the life of the process.  A call holds its device's lock while it
+// enqueues, so calls from several host threads take turns; an event recorded again by a later
+// call is safe, because each stream wait binds to the event's most recent record at the time
+// the wait is enqueued.
+struct HostStepResources {
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    std::vector<cudaEvent_t> events;
+};
+HostStepResources g_host_step[kHostStepDevices];
+std::mutex g_host_step_mutex[kHostStepDevices];
+
+// The streams of device `dev` (current) and at least `n` events; false on a CUDA error.
+bool host_step_resources(int dev, size_t n, HostStepResources **out) {
+    HostStepResources &r = g_host_step[dev];
+    if (!r.ready) {
+        if (cudaStreamCreateWithFlags(&r.s_in, cudaStreamNonBlocking) != cudaSuccess) return false;
+        if (cudaStreamCreateWithFlags(&r.s_out, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaStreamDestroy(r.s_in);
+            r.s_in = nullptr;
+            return false;
+        }
+        r.ready = true;
+    }
+    while (r.events.size() < n) {
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return false;
+        r.events.push_back(e);
+    }
+    *out = &r;
+    return true;
+}
+
 }  // namespace
 }  // namespace tsa
 
@@ -635,19 +673,21 @@ tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const voi
     DeviceFlags flags;
     TSA_TRY(device_flags(dev, &flags));
 
-    // Two copy streams beside the caller's: host-to-device (K first, then Q and V) and
-    // device-to-host (O).  The work itself runs on the caller's stream.  Streams and events are
-    // released right after enqueueing; CUDA keeps them until their work has completed.
-    cudaStream_t s_in = nullptr, s_out = nullptr;
-    std::vector<cudaEvent_t> ev;
-    auto cleanup = [&]() {
-        for (cudaEvent_t e : ev) cudaEventDestroy(e);
-        if (s_in) cudaStreamDestroy(s_in);
-        if (s_out) cudaStreamDestroy(s_out);
-    };
+    // Two copy streams beside the caller's, the library's own (created once per device):
+    // host-to-device (K first, then Q and V) and device-to-host (O).  The work itself runs on
+    // the caller's stream.
+    if (dev >= kHostStepDevices) return TSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_host_step_mutex[dev]);
+    HostStepResources *res = nullptr;
+    const size_t n_events = (size_t)(3 * nchunks + 3);
+    if (!host_step_resources(dev, n_events, &res)) {
+        cudaGetLastError();
+        return TSA_ERR_CUDA;
+    }
+    cudaStream_t s_in = res->s_in, s_out = res->s_out;
+    size_t next_event = 0;
     auto event = [&](cudaEvent_t *e) {
-        if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
-        ev.push_back(*e);
+        *e = res->events[next_event++];
         return true;
     };
     const size_t lane_bytes = (size_t)(S * D) * 2;
@@ -655,8 +695,7 @@ tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const voi
         return static_cast<const uint8_t *>(base) + (size_t)(c * lc) * lane_bytes;
     };
     auto chunk_lanes = [&](int64_t c) { return (c + 1) * lc <= lanes ? lc : lanes - c * lc; };
-    bool ok = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking) == cudaSuccess &&
-              cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking) == cudaSuccess;
+    bool ok = true;
     cudaEvent_t e_start = nullptr, e_end = nullptr;
     ok = ok && event(&e_start) && event(&e_end) && cudaEventRecord(e_start, st) == cudaSuccess &&
          cudaStreamWaitEvent(s_in, e_start, 0) == cudaSuccess && cudaStreamWaitEvent(s_out, e_start, 0) == cudaSuccess;
@@ -718,14 +757,13 @@ tsa_status tsa_topology_attention_host(const void *hQ, const void *hK, const voi
             status = TSA_ERR_CUDA;
     }
     // the caller's stream continues once every copy has been made
-    if (s_in && s_out && e_end) {
+    if (e_end) {
         cudaEvent_t e_in = nullptr;
         if (!event(&e_in) || cudaEventRecord(e_in, s_in) != cudaSuccess ||
             cudaStreamWaitEvent(s_out, e_in, 0) != cudaSuccess || cudaEventRecord(e_end, s_out) != cudaSuccess ||
             cudaStreamWaitEvent(st, e_end, 0) != cudaSuccess)
             status = TSA_ERR_CUDA;
     }
-    cleanup();
     if (status != TSA_OK) cudaGetLastError();
     return status;
 }

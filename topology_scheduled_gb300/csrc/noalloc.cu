@@ -6,6 +6,8 @@
 // name as a device address (in host code it names a host-side stand-in), so the first call on
 // each device looks the device address up with cudaGetSymbolAddress, with that device
 // current, and caches it.
+#include <climits>
+#include <cstdint>
 #include <mutex>
 
 #include "tsa_internal.h"
@@ -45,9 +47,16 @@ extern "C" tsa_status tsa_build_schedule_noalloc(const void *K, tsa_dtype dtype,
                                                  int32_t *col_idx, int64_t col_cap,
                                                  double *salience_sq, tsa_stream_t stream) {
     if (!K || !row_ptr || !col_idx) return TSA_ERR_INVALID_ARGUMENT;
-    // Same scratch layout as the workspace of tsa_build_schedule; 0 means invalid arguments,
-    // which tsa_build_schedule reports below with its own status.
+    // The callee's size checks, repeated before the scratch need is computed: the array is
+    // shared by every call on the device, so a size that wrapped around must never pass the
+    // capacity test below.
+    if (lanes <= 0 || S <= 0 || D <= 0 || block <= 0) return TSA_ERR_INVALID_ARGUMENT;
+    const int64_t nb = (S + block - 1) / block;
+    if (nb > tsa::kMaxScheduleBlocks || D > tsa::kMaxScheduleDim) return TSA_ERR_UNSUPPORTED;
+    if (lanes > INT64_MAX / S / D || lanes > INT64_MAX / 16 / nb / D) return TSA_ERR_INVALID_ARGUMENT;
+    // Same scratch layout as the workspace of tsa_build_schedule.
     const size_t need = tsa_build_schedule_workspace_bytes(lanes, S, D, block);
+    if (need == 0) return TSA_ERR_INVALID_ARGUMENT;
     if (need > (size_t)TSA_NOALLOC_SCRATCH_BYTES) return TSA_ERR_CAPACITY;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) {
