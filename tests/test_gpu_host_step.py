@@ -3,12 +3,15 @@ Its O and CSR must equal, bit for bit, those of the device-resident calls it cha
 (tsa_build_schedule_ex and tsa_scheduled_attention on the same inputs), for every lane-chunk
 size (one lane per chunk, uneven chunks, the default, one chunk), both dtypes and head dims, a
 partial last block, page-locked and pageable host memory; a device pointer given as host memory
-is refused."""
+is refused.  One case per dtype is also compared directly with the oracle (fp64 CPU): the CSR
+bit for bit, O on every row within the attention tolerance."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import topology_scheduled_gb300 as tsa
+from _tol import assert_close
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -67,3 +70,18 @@ def test_device_pointer_as_host_is_refused():
                                        256, 64, 64, 1, 1, 2, 0, 0.125, *[b.data_ptr() for b in bufs],
                                        rp.data_ptr(), ci.data_ptr(), ci.numel(), ws.data_ptr(), ws.numel(), 0, None)
     assert st == 1
+
+
+@pytest.mark.parametrize("L,S,D,dtype,block,tie", [(6, 2048, 128, torch.bfloat16, 64, "index"),
+                                                    (5, 1000, 64, torch.float16, 64, "content")])
+def test_equals_oracle(L, S, D, dtype, block, tie):
+    hq, hk, hv = _inputs(L, S, D, dtype, 7 * S + L)
+    hk = (hk.float() * 2.5).to(dtype)  # wider spread of the key-block centroids
+    out, rp, ci = tsa.tsa_topology_attention_host(hq, hk, hv, block, 2, 2, 3, tie_break=tie, lane_chunk=2)
+    torch.cuda.synchronize()
+    assert tsa.tsa_last_device_status() == 0
+    orp, oci, _ = oracle.build_schedule(hk, block, 2, 2, 3, tie=tie)
+    rp = rp.cpu().numpy()
+    assert np.array_equal(rp, orp) and np.array_equal(ci.cpu().numpy()[: rp[-1]], oci)
+    ref = oracle.attention(hq, hk, hv, orp, oci, block, D ** -0.5, nthreads=8)
+    assert_close(out.double().numpy(), ref, dtype)

@@ -2,8 +2,8 @@
 
 Schedule builder and dense CSR: bit-exact against the oracle (nb = ceil(S / 64), the last
 block's centroid averages the tokens it holds).  Attention: element by element against the
-oracle within the tolerance of test_gpu_attention (2e-3 fp16, 1e-2 bf16, one output ulp where
-the format is coarser), every lane compared, so a partial block that wrote past its lane's last
+oracle within the tolerance of test_gpu_attention (2e-3 fp16, 1e-2 bf16; the bound plus half an
+output ulp where the format is coarser), every lane compared, so a partial block that wrote past its lane's last
 row into the next lane would show; rows past the last lane's end and log-sum-exp entries past
 the end stay untouched.  Backward: dQ, dK, dV against the oracle within test_gpu_backward's
 tolerance, with the same untouched-tail check.

@@ -1,10 +1,13 @@
 """The schedule build in two halves (tsa_block_sums, tsa_build_schedule_from_sums), as a
 lane-sharded build runs it: block sums of each shard of lanes, concatenated in lane order, give
-the CSR and salience of the one-call build bit for bit.  One GPU plays every shard."""
+the oracle's CSR and salience (fp64 CPU, Kruskal) bit for bit, and so the one-call build's.
+One GPU plays every shard here; tests/test_gpu_lane_sharded_procs.py runs the shards in
+separate processes with a real exchange."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import topology_scheduled_gb300 as tsa
 from topology_scheduled_gb300.workloads import WORKLOADS, make_qkv
 
@@ -34,6 +37,20 @@ def test_sharded_build_equals_one_call(name, tie, cuts):
     a, b = _csr(rp, ci), _csr(rp2, ci2)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
     assert torch.equal(sal.view(torch.int64), sal2.view(torch.int64))
+    # against the oracle on the same keys (computed once per workload and tie rule)
+    orp, oci, osal = _oracle_schedule(name, tie, k)
+    assert np.array_equal(b[0], orp) and np.array_equal(b[1], oci)
+    assert np.array_equal(sal2.cpu().numpy().view(np.uint64), osal.view(np.uint64))
+
+
+_ORACLE = {}
+
+
+def _oracle_schedule(name, tie, k):
+    if (name, tie) not in _ORACLE:
+        w = WORKLOADS[name]
+        _ORACLE[(name, tie)] = oracle.build_schedule(k.cpu(), w.block, w.sink, w.local_radius, w.topk, tie=tie)
+    return _ORACLE[(name, tie)]
 
 
 def test_block_sums_are_the_block_sums():

@@ -193,11 +193,13 @@ def tsa_block_sums(K: torch.Tensor, block: int = 64, *, out: torch.Tensor | None
 def tsa_build_schedule_from_sums(sums: torch.Tensor, block: int = 64, sink: int = 1, local_radius: int = 1,
                                  topk: int = 2, *, S: int | None = None, salience: bool = False,
                                  tie_break: str = "index", workspace: torch.Tensor | None = None,
+                                 row_ptr: torch.Tensor | None = None, col_idx: torch.Tensor | None = None,
                                  stream=None):
     """tsa_build_schedule from the block sums of all lanes ([lanes, nb, D] float64, lanes in
     global order, e.g. gathered from the GPUs that hold them).  Same result as
     tsa_build_schedule on the full keys, bit for bit.  S is the sequence length (default
-    nb * block; give it when the last block is partial)."""
+    nb * block; give it when the last block is partial).  row_ptr / col_idx, if given, receive
+    the CSR (int32 CUDA tensors of nb + 1 and at least tsa_schedule_max_nnz entries)."""
     if not sums.is_cuda or not sums.is_contiguous() or sums.dtype != torch.float64 or sums.dim() != 3:
         raise ValueError("sums must be a contiguous CUDA float64 tensor [lanes, nb, D]")
     if tie_break not in TIE_RULES:
@@ -217,8 +219,15 @@ def tsa_build_schedule_from_sums(sums: torch.Tensor, block: int = 64, sink: int 
     dev = sums.device
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
-    col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    if row_ptr is None:
+        row_ptr = torch.empty(nb + 1, dtype=torch.int32, device=dev)
+    if col_idx is None:
+        col_idx = torch.empty(max(cap, 1), dtype=torch.int32, device=dev)
+    for t in (row_ptr, col_idx):
+        if t.dtype != torch.int32 or not t.is_contiguous() or t.device != dev:
+            raise ValueError("row_ptr / col_idx must be contiguous int32 tensors on the sums' device")
+    if row_ptr.numel() != nb + 1:
+        raise ValueError("row_ptr must hold nb + 1 entries")
     sal = torch.empty(nb, dtype=torch.float64, device=dev) if salience else None
     _check(L.tsa_build_schedule_from_sums(sums.data_ptr(), lanes, S, D, block, sink, local_radius, topk,
                                           TIE_RULES[tie_break], row_ptr.data_ptr(), col_idx.data_ptr(),
