@@ -94,6 +94,22 @@ def test_wide_score_range_exercises_rescaling():
     _compare_full(q, k, v, rp, ci, D ** -0.5)
 
 
+@pytest.mark.parametrize("dtype,growth", [(torch.float16, 4.0), (torch.bfloat16, 8.0)])
+def test_running_maximum_grows_past_the_rescale_threshold(dtype, growth):
+    """Key block j scaled by growth * (j + 1): each block's row maxima exceed the previous ones
+    by more than the lazy-rescale threshold (2^15 for f16, 2^30 for bf16), so the kernel must
+    rescale O and the denominator many times along every dense row."""
+    S, D = 1024, 64
+    g = torch.Generator().manual_seed(77)
+    q = torch.randn((2, S, D), generator=g)
+    kscale = growth * (torch.arange(S) // 64 + 1).float().view(1, S, 1)
+    k = torch.randn((2, S, D), generator=g) * kscale
+    v = torch.randn((2, S, D), generator=g)
+    q, k, v = (x.to(dtype) for x in (q, k, v))
+    rp, ci = oracle.dense_causal_csr(S // 64)
+    _compare_full(q, k, v, rp, ci, D ** -0.5)
+
+
 def test_four_dim_input_and_dtype_preserved():
     g = torch.Generator().manual_seed(3)
     q, k, v = (torch.randn((2, 3, 256, 64), generator=g).to(torch.bfloat16) for _ in range(3))

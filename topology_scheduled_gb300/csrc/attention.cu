@@ -24,9 +24,9 @@
 //    row union), p_full (softmax -> MMA), o_done (PV completion, for rescaling and the
 //    epilogue).
 //  * Lazy rescale.  O and the denominator are rescaled only when a row's maximum grows by more
-//    than 2^8; the final O / l uses the same stale maximum, so the result is unchanged.  The
-//    decision is per row but TMEM loads/stores are warp-collective, so a warp rescales when
-//    any of its rows must (factor 1 for the others).
+//    than 2^30 (bf16) or 2^15 (f16); the final O / l uses the same stale maximum, so the result
+//    is unchanged.  The decision is per row but TMEM loads/stores are warp-collective, so a
+//    warp rescales when any of its rows must (factor 1 for the others).
 //  * Epilogue.  O / l rounded to the input dtype, staged in the Q tile, TMA-stored per block;
 //    optionally the row's log-sum-exp (m + log l), which the backward pass recomputes P from.
 //  * Partial last block (S not a multiple of 64).  Its key rows past S are read but never
@@ -51,7 +51,13 @@ constexpr int kVStages = 2;           // V ring depth
 constexpr int kThreads = 192;         // 4 softmax warps + producer warp + MMA warp
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr float kRescaleLog2 = 8.0f;  // lazy-rescale threshold (log2 units)
+// Lazy-rescale threshold (log2 units): O and the denominator are rescaled only when a row's
+// maximum grows past the one they are scaled to by more than this, so p stays at most 2^30
+// (bf16: far inside its range and the fp32 accumulators') or 2^15 (f16: below its largest
+// finite value, 65504).  Rescales cost a wait for the running PV product and a pass over O in
+// TMEM; keys drawn around distinct cluster means made a small threshold (2^8) rescale often.
+template <bool kBF16>
+__device__ __forceinline__ constexpr float rescale_log2() { return kBF16 ? 30.0f : 15.0f; }
 
 template <int D>
 struct AttnSmem {
@@ -587,7 +593,7 @@ scheduled_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const float m7b = max3f(max3f(m21[9], m21[10], m21[11]), max3f(m21[12], m21[13], m21[14]),
                                         max3f(m21[15], m21[16], m21[17]));
                 const float mx = max3f(m7a, m7b, max3f(m21[18], m21[19], fmaxf(m21[20], m21[21]))) * scale_log2;
-                const bool grow = mx > m_used + kRescaleLog2;
+                const bool grow = mx > m_used + rescale_log2<kBF16>();
                 if (__any_sync(0xffffffffu, grow)) {
                     const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : ex2_approx(m_used - mx));
                     if (u > 0) {
