@@ -327,7 +327,8 @@ centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S
                 hi[i] = s;
                 const uint32_t a = x & 0x7FFF7FFFu;
                 mx[i] = __vmaxu2(mx[i], a);
-                mn[i] = __vminu2(mn[i], a | __vcmpeq2(a, 0u));
+                // minimum of |bits| - 1 per half: a zero wraps to 0xFFFF and never lowers it
+                mn[i] = __vminu2(mn[i], __vsub2(a, 0x00010001u));
             } else {
                 col_add(cs[2 * i], x & 0xFFFFu, false);
                 col_add(cs[2 * i + 1], x >> 16, false);
@@ -375,7 +376,8 @@ centroid_partial_stream(const uint16_t *__restrict__ K, int64_t lanes, int64_t S
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t amax = (mx[i] >> (16 * h)) & 0xFFFFu;
-                    const uint32_t amin = (mn[i] >> (16 * h)) & 0xFFFFu;
+                    const uint32_t amin_m1 = (mn[i] >> (16 * h)) & 0xFFFFu;
+                    const uint32_t amin = amin_m1 == 0xFFFFu ? 0xFFFFu : amin_m1 + 1u;  // 0xFFFF: all zero
                     const int emax = (int)(amax >> kMantBits);
                     const int emin = max(1, (int)(amin >> kMantBits));
                     const bool all_zero = amin == 0xFFFFu;
