@@ -79,7 +79,7 @@ def test_other_blocks_unsupported():
 def test_backward_block128_matches_oracle(L, S, D, dtype, kind):
     """dQ, dK, dV over a CSR of 128-token blocks (expanded on the GPU to the 64-token CSR with
     the same allowed keys) against the oracle at block 128, test_gpu_backward's tolerance."""
-    from test_gpu_backward import U, _close
+    from test_gpu_backward import ETA, U, _bounds, _close
     g = torch.Generator().manual_seed(S + 7 * D + L)
     q, k, v, dO = (torch.randn((L, S, D), generator=g).to(dtype) for _ in range(4))
     nb = -(-S // 128)
@@ -108,8 +108,9 @@ def test_backward_block128_matches_oracle(L, S, D, dtype, kind):
                                                  scale, block=128)
     assert tsa.tsa_last_device_status() == 0
     refs = oracle.attention_backward(q, k, v, dO, rp, ci, 128, scale, nthreads=8)
-    for name, got, ref in zip(("dQ", "dK", "dV"), grads, refs):
-        _close(got, ref, U[dtype], f"{kind} {name}")
+    bounds = _bounds(q, k, v, dO, rp, ci, scale, U[dtype], ETA[dtype], block=128)
+    for name, got, ref, b in zip(("dQ", "dK", "dV"), grads, refs, bounds):
+        _close(got, ref, U[dtype], f"{kind} {name}", b, ETA[dtype])
 
 
 def test_backward_block128_bad_schedule_is_reported():

@@ -15,7 +15,7 @@ import torch
 import oracle
 import topology_scheduled_gb300 as tsa
 from test_gpu_attention import assert_close
-from test_gpu_backward import U, _close, _schedule
+from test_gpu_backward import ETA, U, _bounds, _close, _schedule
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -107,5 +107,6 @@ def test_backward_matches_oracle(L, S, D, dtype, kind):
     for b in bufs:
         assert bool((b[L * S:] == 7.0).all())
     refs = oracle.attention_backward(q, k, v, dO, rp, ci, 64, scale, nthreads=8)
-    for name, got, ref in zip(("dQ", "dK", "dV"), grads, refs):
-        _close(got, ref, U[dtype], f"{kind} {name}")
+    bounds = _bounds(q, k, v, dO, rp, ci, scale, U[dtype], ETA[dtype])
+    for name, got, ref, b in zip(("dQ", "dK", "dV"), grads, refs, bounds):
+        _close(got, ref, U[dtype], f"{kind} {name}", b, ETA[dtype])
