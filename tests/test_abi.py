@@ -89,6 +89,34 @@ def test_host_checks_before_any_device_call():
                                 1 << 40, None) == 2
 
 
+def test_noalloc_host_checks_before_any_device_call():
+    """The allocation-free builder refuses bad or oversized arguments on the host, before it
+    looks up its device array: the callee's own size checks come first (so a size that wrapped
+    around can never pass the capacity test), then the scratch capacity."""
+    L = tsa.lib()
+    fake = ctypes.c_void_p(4096)
+
+    def call(K, lanes, S, D, block, row_ptr=fake, col_idx=fake):
+        return L.tsa_build_schedule_noalloc(K, 0, lanes, S, D, block, 1, 1, 2, row_ptr, col_idx, 1 << 20,
+                                            None, None)
+
+    assert call(None, 1, 1024, 64, 64) == 1                    # null keys
+    assert call(fake, 1, 1024, 64, 64, row_ptr=None) == 1     # null row_ptr
+    assert call(fake, 1, 1024, 64, 64, col_idx=None) == 1     # null col_idx
+    assert call(fake, 0, 1024, 64, 64) == 1                    # no lanes
+    assert call(fake, 1, 0, 64, 64) == 1                       # empty sequence
+    assert call(fake, 1, 1024, 0, 64) == 1                     # empty head dimension
+    assert call(fake, 1, 1024, 64, 0) == 1                     # zero block
+    assert call(fake, 1, 64 * 4097, 64, 64) == 2               # beyond 4096 blocks
+    assert call(fake, 1, 1024, 4096, 64) == 2                  # head dimension beyond the builder's
+    # lanes * S * D past int64: refused as invalid, never wrapped into a small scratch need
+    assert call(fake, 1 << 50, 1 << 10, 1 << 10, 64) == 1
+    assert tsa.tsa_build_schedule_workspace_bytes(1 << 50, 1 << 10, 1 << 10, 64) == 0
+    # a valid workload larger than the 16 MiB array
+    assert tsa.tsa_build_schedule_workspace_bytes(64, 32768, 128, 64) > 16 << 20
+    assert call(fake, 64, 32768, 128, 64) == 5
+
+
 def test_fixed_segment_nnz_closed_form():
     # the mirror page's counts at S 4096, block 64: 288 (512-token), 160 (256-token), 2080 dense
     assert tsa.tsa_fixed_segment_nnz(4096, 64, 512) == 288
