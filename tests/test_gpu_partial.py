@@ -66,7 +66,9 @@ def _attention(q, k, v, rp, ci, scale, rows_extra=64):
 
 @pytest.mark.parametrize("L,S,D,dtype", [(1, 100, 64, torch.float16), (3, 1000, 128, torch.bfloat16),
                                          (4, 130, 128, torch.float16), (2, 4133, 64, torch.bfloat16),
-                                         (1, 8191, 128, torch.bfloat16)])
+                                         (1, 8191, 128, torch.bfloat16),
+                                         # one query block, partial: one token, and 63 tokens
+                                         (1, 1, 64, torch.float16), (3, 63, 128, torch.bfloat16)])
 @pytest.mark.parametrize("kind", ["dense", "topology"])
 def test_attention_matches_oracle(L, S, D, dtype, kind):
     q, k, v = _qkv(L, S, D, dtype, S + D)
@@ -84,6 +86,7 @@ def test_attention_matches_oracle(L, S, D, dtype, kind):
 
 
 @pytest.mark.parametrize("L,S,D,dtype,kind", [(1, 100, 64, torch.float16, "dense"),
+                                              (2, 33, 64, torch.float16, "dense"),
                                                 (3, 1000, 128, torch.bfloat16, "random"),
                                                 (2, 4133, 64, torch.bfloat16, "holes"),
                                                 (2, 130, 128, torch.float16, "dense"),
